@@ -1,0 +1,172 @@
+/*
+ * sage_gb300.h - C ABI of the GB300 (sm_103a) quantized exact attention library.
+ *
+ * The library implements the numerical contract whose stages the Experiment
+ * Log lists under "Phase 0 Import And Verification": Q/K preparation, K
+ * smoothing, INT8 quantization, QK traversal, online softmax, FP8 V/P,
+ * two-level PV accumulation, final conversion and ragged tails; with the
+ * strict tile order, exact FP8 score bytes and per-tile RO rescaling named
+ * under "Phase 1 State-Ownership Decision", and the checkpoint list (QK, m,
+ * d, FP8 probability, rescale, FP16 PV, FP32 RO, reciprocal, BF16 output) of
+ * "Phase 2B Fixed Aligned Numerical Prototype".  Strided NHD views of a fused
+ * projection buffer are accepted directly (Experiment Registry, "Complete
+ * Registry", row qkv-direct-sageattention-layout); the library never makes a
+ * padded copy (row layout-direct-q-padding-32) and never allocates on the hot
+ * path (row layout-dynamic-to-hot-allocation).
+ *
+ * Conventions for every entry point:
+ *  - All buffers are caller-owned.  Device pointers must be device memory of
+ *    the current CUDA device; host pointers (sage_attention_host only) should
+ *    be pinned for asynchronous copies.  The library allocates nothing, frees
+ *    nothing and does not synchronize, except sage_get_device_status.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Work is enqueued on it; results are ready when the stream completes.
+ *  - Return value: SAGE_OK (0) when the work was enqueued, or a negative
+ *    SAGE_ERR_* code when arguments were rejected (nothing enqueued) or the
+ *    launch failed.  Errors found on the device (a bounded wait that ran out)
+ *    are recorded in a device status word read by sage_get_device_status.
+ *  - Only D = 128 is supported.  Q, K, V and O are BF16.
+ */
+#ifndef SAGE_GB300_H
+#define SAGE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum sage_status {
+    SAGE_OK = 0,
+    SAGE_ERR_ARG = -1,          /* null pointer, non-positive size, bad length */
+    SAGE_ERR_UNSUPPORTED = -2,  /* D != 128, misaligned pointer or stride */
+    SAGE_ERR_LAUNCH = -3,       /* CUDA reported an error at launch */
+    SAGE_ERR_TIMEOUT = -4,      /* device: a bounded wait inside a kernel ran out */
+    SAGE_ERR_DRIVER = -5        /* driver entry point for TMA descriptors missing */
+};
+
+/* Logical [B, H, N, D] BF16 tensor given by its element strides; the D stride
+ * is 1.  NHD ([B,N,H,D]) and HND ([B,H,N,D]) layouts and strided views into a
+ * fused QKV buffer are all described this way.  ptr and the three strides
+ * (in bytes) must be multiples of 16 bytes. */
+typedef struct {
+    const void* ptr;
+    int64_t stride_b;
+    int64_t stride_h;
+    int64_t stride_n;
+} sage_tensor;
+
+/* Outputs of sage_prep_qkv / inputs of sage_attn_fwd (all device memory).
+ * Sizes are given by sage_buffer_sizes.  Nkv_pad = Nkv rounded up to 16.
+ *   q16     fp16 [B, H, Nq, D]      INT8 Q codes held as exact FP16 integers
+ *   k16     fp16 [B, H, Nkv, D]     INT8 codes of the smoothed K, as FP16
+ *   v8t     e4m3 [B, H, D, Nkv_pad] FP8 V codes, token index fastest
+ *   q_scale f32  [B, H, ceil(Nq/128)]  per 128-row Q block
+ *   k_scale f32  [B, H, ceil(Nkv/64)]  per 64-row K block
+ *   v_scale f32  [B, H, D]          per channel
+ *   k_mean  f32  [B, H, D]          channel mean removed from K
+ *   q8, k8  int8 [B, H, Nq|Nkv, D]  optional INT8 code bytes (NULL: skipped)
+ *   workspace                       scratch of sage_buffer_sizes().workspace
+ * Rows at or beyond a batch item's valid length are written as code 0 and
+ * scales of blocks holding no valid row are 0, so no uninitialised byte is
+ * ever read by sage_attn_fwd. */
+typedef struct {
+    uint16_t* q16;
+    uint16_t* k16;
+    uint8_t* v8t;
+    float* q_scale;
+    float* k_scale;
+    float* v_scale;
+    float* k_mean;
+    int8_t* q8;
+    int8_t* k8;
+    void* workspace;
+    size_t workspace_bytes;
+} sage_prep_buffers;
+
+typedef struct {
+    size_t q16, k16, v8t, q_scale, k_scale, v_scale, k_mean, q8, k8, workspace;
+    int64_t nkv_pad;
+} sage_sizes;
+
+/* Byte sizes of every buffer of sage_prep_buffers for a problem shape.
+ * Returns SAGE_ERR_ARG / SAGE_ERR_UNSUPPORTED for bad shapes. */
+int sage_buffer_sizes(int B, int H, int Nq, int Nkv, int D, sage_sizes* out);
+
+/* Preparation (Experiment Log, "Phase 0 Import And Verification": Q/K
+ * preparation, K smoothing, INT8 quantization, FP8 V).
+ *  q, k, v : BF16 inputs [B,H,Nq,D], [B,H,Nkv,D], [B,H,Nkv,D] (device).
+ *  q_len, kv_len : device int32 [B] valid lengths (<= Nq, <= Nkv), or NULL
+ *                  for all rows valid.  Out-of-range lengths are clamped.
+ *  out : device buffers, filled completely (see sage_prep_buffers).
+ * Steps: per (b,h,channel) mean of the valid keys in a fixed order (chunks of
+ * 64 tokens summed in order, chunk sums in order, one division); K - mean;
+ * per-block amax, scale = amax/127, codes rne(x*127/amax); V per channel to
+ * e4m3 with scale amax/1.125.  Enqueues three kernels. */
+int sage_prep_qkv(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
+                  int B, int H, int Nq, int Nkv, int D,
+                  const int32_t* q_len, const int32_t* kv_len,
+                  const sage_prep_buffers* out, void* stream);
+
+/* Fused attention (QK traversal through FP32 running output and BF16
+ * conversion).  `in` holds the output of sage_prep_qkv for the same shape and
+ * lengths.  o : BF16 [B,H,Nq,D] output (device); rows >= q_len[b] are not
+ * written; rows of a batch item with kv_len = 0 are written as zero.
+ * sm_scale <= 0 selects 1/sqrt(D).  One kernel: per 128-row query tile, a TMA
+ * producer warp, a single-thread tcgen05 MMA issuer (QK on FP16 integer codes
+ * with FP32 accumulation, PV as e4m3 x e4m3 with P taken from tensor memory),
+ * a softmax warpgroup and a correction/epilogue warpgroup. */
+int sage_attn_fwd(const sage_prep_buffers* in, const sage_tensor* o,
+                  int B, int H, int Nq, int Nkv, int D,
+                  const int32_t* q_len, const int32_t* kv_len,
+                  float sm_scale, void* stream);
+
+/* The "QK" checkpoint: exact integer scores S[b,h,i,j] = sum_d q8*k8 from the
+ * same tensor-core path sage_attn_fwd uses, written as int32 to
+ * s [B, H, Nq, Nkv] (device, row-major).  Entries with i >= q_len[b] or
+ * j >= kv_len[b] are not written. */
+int sage_qk_int32(const sage_prep_buffers* in, int32_t* s,
+                  int B, int H, int Nq, int Nkv, int D,
+                  const int32_t* q_len, const int32_t* kv_len, void* stream);
+
+/* One host<->device region copied with one cudaMemcpyAsync. */
+typedef struct {
+    const void* host;
+    void* device;
+    size_t bytes;
+} sage_copy;
+
+/* End-to-end call from host memory: copies every `inputs` region host->device,
+ * runs sage_prep_qkv and sage_attn_fwd on the device views q, k, v, o (which
+ * point into those regions), then copies `output` device->host, all on
+ * `stream`, without synchronizing.  Lengths are taken as all-valid. */
+int sage_attention_host(const sage_copy* inputs, int n_inputs,
+                        const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
+                        const sage_prep_buffers* buf, const sage_tensor* o,
+                        const sage_copy* output,
+                        int B, int H, int Nq, int Nkv, int D, float sm_scale, void* stream);
+
+/* Synchronizes the device, returns the first error a kernel recorded since
+ * the last call (SAGE_OK if none) and clears it. */
+int sage_get_device_status(void);
+
+/* Static description of a status code. */
+const char* sage_status_string(int code);
+
+/* Number of kernel launches the last successful sage_prep_qkv / sage_attn_fwd
+ * call enqueued (for launch accounting). */
+int sage_last_launch_count(void);
+
+/* Test hook for the failure-detection tests: mode 1 makes the next
+ * sage_attn_fwd launch withhold its V tile copies, so the MMA issuer's
+ * bounded wait runs out, the kernel records SAGE_ERR_TIMEOUT, releases its
+ * tensor memory and returns; mode 0 restores normal launches.  Use only on
+ * a problem of one or a few query tiles (each CTA waits about one second). */
+int sage_debug_inject_fault(int mode);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SAGE_GB300_H */

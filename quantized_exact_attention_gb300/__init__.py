@@ -1,0 +1,246 @@
+"""GB300 (sm_103a) quantized exact attention: Python binding of libsage_gb300.so.
+
+This module only marshals arguments for the C ABI declared in
+``include/sage_gb300.h``; every step of the computation runs in the CUDA
+kernels of the shared library.  PyTorch is used to allocate device memory and
+to hand over CUDA streams.  There is no CPU fallback: if the compiled library
+is missing, loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libsage_gb300.so")
+
+SAGE_OK = 0
+SAGE_ERR_ARG = -1
+SAGE_ERR_UNSUPPORTED = -2
+SAGE_ERR_LAUNCH = -3
+SAGE_ERR_TIMEOUT = -4
+SAGE_ERR_DRIVER = -5
+
+D_HEAD = 128
+
+# Names the header declares (checked by the CPU tests against the .so exports).
+EXPORTED = ("sage_buffer_sizes", "sage_prep_qkv", "sage_attn_fwd", "sage_qk_int32",
+            "sage_attention_host", "sage_get_device_status", "sage_status_string",
+            "sage_last_launch_count", "sage_debug_inject_fault")
+
+
+class SageError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {status_string(code)} ({code})")
+        self.code = code
+
+
+class sage_tensor(ctypes.Structure):
+    _fields_ = [("ptr", ctypes.c_void_p), ("stride_b", ctypes.c_int64),
+                ("stride_h", ctypes.c_int64), ("stride_n", ctypes.c_int64)]
+
+
+class sage_prep_buffers(ctypes.Structure):
+    _fields_ = [("q16", ctypes.c_void_p), ("k16", ctypes.c_void_p), ("v8t", ctypes.c_void_p),
+                ("q_scale", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
+                ("v_scale", ctypes.c_void_p), ("k_mean", ctypes.c_void_p),
+                ("q8", ctypes.c_void_p), ("k8", ctypes.c_void_p),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+
+
+class sage_sizes(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in
+                ("q16", "k16", "v8t", "q_scale", "k_scale", "v_scale", "k_mean", "q8", "k8",
+                 "workspace")] + [("nkv_pad", ctypes.c_int64)]
+
+
+class sage_copy(ctypes.Structure):
+    _fields_ = [("host", ctypes.c_void_p), ("device", ctypes.c_void_p), ("bytes", ctypes.c_size_t)]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the compiled library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libsage_gb300.so not found at {path}; run quantized_exact_attention_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    P = ctypes.POINTER
+    i, vp, f = ctypes.c_int, ctypes.c_void_p, ctypes.c_float
+    lib.sage_buffer_sizes.argtypes = [i, i, i, i, i, P(sage_sizes)]
+    lib.sage_prep_qkv.argtypes = [P(sage_tensor), P(sage_tensor), P(sage_tensor), i, i, i, i, i, vp, vp,
+                                  P(sage_prep_buffers), vp]
+    lib.sage_attn_fwd.argtypes = [P(sage_prep_buffers), P(sage_tensor), i, i, i, i, i, vp, vp, f, vp]
+    lib.sage_qk_int32.argtypes = [P(sage_prep_buffers), vp, i, i, i, i, i, vp, vp, vp]
+    lib.sage_attention_host.argtypes = [P(sage_copy), i, P(sage_tensor), P(sage_tensor), P(sage_tensor),
+                                        P(sage_prep_buffers), P(sage_tensor), P(sage_copy),
+                                        i, i, i, i, i, f, vp]
+    lib.sage_get_device_status.argtypes = []
+    lib.sage_status_string.argtypes = [i]
+    lib.sage_status_string.restype = ctypes.c_char_p
+    lib.sage_last_launch_count.argtypes = []
+    lib.sage_debug_inject_fault.argtypes = [i]
+    for name in EXPORTED:
+        if name != "sage_status_string":
+            getattr(lib, name).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return load_library().sage_status_string(int(code)).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != SAGE_OK:
+        raise SageError(rc, what)
+
+
+def _stream_ptr(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream or None
+
+
+def tensor_desc(t: torch.Tensor) -> sage_tensor:
+    """Describe a logical [B, H, N, D] BF16 view (any strides, D stride 1)."""
+    if t.dim() != 4 or t.dtype != torch.bfloat16 or t.stride(3) != 1:
+        raise ValueError("expected a [B, H, N, D] bfloat16 view with unit D stride")
+    return sage_tensor(t.data_ptr(), t.stride(0), t.stride(1), t.stride(2))
+
+
+def buffer_sizes(B: int, H: int, Nq: int, Nkv: int, D: int = D_HEAD) -> sage_sizes:
+    s = sage_sizes()
+    _check(load_library().sage_buffer_sizes(B, H, Nq, Nkv, D, ctypes.byref(s)), "sage_buffer_sizes")
+    return s
+
+
+@dataclass
+class PrepBuffers:
+    """Device buffers of sage_prep_buffers, allocated by torch."""
+    q16: torch.Tensor
+    k16: torch.Tensor
+    v8t: torch.Tensor
+    q_scale: torch.Tensor
+    k_scale: torch.Tensor
+    v_scale: torch.Tensor
+    k_mean: torch.Tensor
+    q8: torch.Tensor | None
+    k8: torch.Tensor | None
+    workspace: torch.Tensor
+    nkv_pad: int
+
+    def c_struct(self) -> sage_prep_buffers:
+        ptr = lambda t: t.data_ptr() if t is not None else None  # noqa: E731
+        return sage_prep_buffers(ptr(self.q16), ptr(self.k16), ptr(self.v8t), ptr(self.q_scale),
+                                 ptr(self.k_scale), ptr(self.v_scale), ptr(self.k_mean),
+                                 ptr(self.q8), ptr(self.k8), ptr(self.workspace),
+                                 self.workspace.numel())
+
+
+def alloc_prep_buffers(B, H, Nq, Nkv, device="cuda", int8_codes=False, D=D_HEAD) -> PrepBuffers:
+    sz = buffer_sizes(B, H, Nq, Nkv, D)
+    pad = int(sz.nkv_pad)
+    e = lambda shape, dt: torch.empty(shape, dtype=dt, device=device)  # noqa: E731
+    return PrepBuffers(
+        q16=e((B, H, Nq, D), torch.float16), k16=e((B, H, Nkv, D), torch.float16),
+        v8t=e((B, H, D, pad), torch.uint8),
+        q_scale=e((B, H, (Nq + 127) // 128), torch.float32),
+        k_scale=e((B, H, (Nkv + 63) // 64), torch.float32),
+        v_scale=e((B, H, D), torch.float32), k_mean=e((B, H, D), torch.float32),
+        q8=e((B, H, Nq, D), torch.int8) if int8_codes else None,
+        k8=e((B, H, Nkv, D), torch.int8) if int8_codes else None,
+        workspace=e((int(sz.workspace),), torch.uint8), nkv_pad=pad)
+
+
+def _lens(x):
+    if x is None:
+        return None
+    assert x.dtype == torch.int32 and x.is_cuda
+    return x.data_ptr()
+
+
+def sage_prep_qkv(q, k, v, bufs: PrepBuffers, q_len=None, kv_len=None, stream=None):
+    """Enqueue the preparation kernels on [B,H,N,D] BF16 views q, k, v."""
+    B, H, Nq, D = q.shape
+    Nkv = k.shape[2]
+    qs, ks, vs, pb = tensor_desc(q), tensor_desc(k), tensor_desc(v), bufs.c_struct()
+    rc = load_library().sage_prep_qkv(ctypes.byref(qs), ctypes.byref(ks), ctypes.byref(vs), B, H, Nq, Nkv, D,
+                                      _lens(q_len), _lens(kv_len), ctypes.byref(pb), _stream_ptr(stream))
+    _check(rc, "sage_prep_qkv")
+
+
+def sage_attn_fwd(bufs: PrepBuffers, o, q_len=None, kv_len=None, sm_scale: float = 0.0, stream=None,
+                  Nkv: int | None = None):
+    """Enqueue the fused attention kernel; o is a [B,H,Nq,D] BF16 view."""
+    B, H, Nq, D = o.shape
+    Nkv = bufs.k16.shape[2] if Nkv is None else Nkv
+    os_, pb = tensor_desc(o), bufs.c_struct()
+    rc = load_library().sage_attn_fwd(ctypes.byref(pb), ctypes.byref(os_), B, H, Nq, Nkv, D,
+                                      _lens(q_len), _lens(kv_len), float(sm_scale), _stream_ptr(stream))
+    _check(rc, "sage_attn_fwd")
+
+
+def sage_qk_int32(bufs: PrepBuffers, s: torch.Tensor, q_len=None, kv_len=None, stream=None):
+    """Enqueue the QK checkpoint kernel; s is int32 [B, H, Nq, Nkv] contiguous."""
+    B, H, Nq, Nkv = s.shape
+    assert s.dtype == torch.int32 and s.is_contiguous()
+    pb = bufs.c_struct()
+    rc = load_library().sage_qk_int32(ctypes.byref(pb), s.data_ptr(), B, H, Nq, Nkv, D_HEAD,
+                                      _lens(q_len), _lens(kv_len), _stream_ptr(stream))
+    _check(rc, "sage_qk_int32")
+
+
+def sage_attention_host(host_phys, dev_phys, views_of, bufs: PrepBuffers, o_dev, o_host,
+                        sm_scale: float = 0.0, stream=None):
+    """End-to-end call: copy host buffers in, prep + attention, copy O out.
+
+    host_phys / dev_phys: matching lists of pinned-host / device tensors
+    holding the physical inputs; views_of(dev_phys) -> (q, k, v) [B,H,N,D]
+    views; o_dev / o_host: device output view and its pinned host twin
+    (same physical layout, contiguous).
+    """
+    q, k, v = views_of(dev_phys)
+    B, H, Nq, D = q.shape
+    Nkv = k.shape[2]
+    n = len(host_phys)
+    copies = (sage_copy * n)(*[sage_copy(h.data_ptr(), d.data_ptr(), h.numel() * h.element_size())
+                              for h, d in zip(host_phys, dev_phys)])
+    out = sage_copy(o_host.data_ptr(), o_dev.data_ptr(), o_host.numel() * o_host.element_size())
+    qs, ks, vs, os_, pb = tensor_desc(q), tensor_desc(k), tensor_desc(v), tensor_desc(o_dev), bufs.c_struct()
+    rc = load_library().sage_attention_host(copies, n, ctypes.byref(qs), ctypes.byref(ks), ctypes.byref(vs),
+                                            ctypes.byref(pb), ctypes.byref(os_), ctypes.byref(out),
+                                            B, H, Nq, Nkv, D, float(sm_scale), _stream_ptr(stream))
+    _check(rc, "sage_attention_host")
+
+
+def sage_get_device_status() -> int:
+    return int(load_library().sage_get_device_status())
+
+
+def sage_last_launch_count() -> int:
+    return int(load_library().sage_last_launch_count())
+
+
+def sage_debug_inject_fault(mode: int):
+    _check(load_library().sage_debug_inject_fault(int(mode)), "sage_debug_inject_fault")
+
+
+def attention(q, k, v, q_len=None, kv_len=None, sm_scale: float = 0.0, out=None, int8_codes=False,
+              stream=None):
+    """Prep + fused attention on [B,H,N,D] BF16 CUDA views; returns (o, bufs)."""
+    B, H, Nq, D = q.shape
+    Nkv = k.shape[2]
+    bufs = alloc_prep_buffers(B, H, Nq, Nkv, q.device, int8_codes=int8_codes)
+    if out is None:
+        out = torch.zeros((B, Nq, H, D), dtype=torch.bfloat16, device=q.device).permute(0, 2, 1, 3)
+    sage_prep_qkv(q, k, v, bufs, q_len, kv_len, stream)
+    sage_attn_fwd(bufs, out, q_len, kv_len, sm_scale, stream, Nkv=Nkv)
+    return out, bufs

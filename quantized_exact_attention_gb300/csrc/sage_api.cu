@@ -1,0 +1,291 @@
+// sage_api.cu - the C ABI declared in include/sage_gb300.h: argument checks,
+// TMA descriptor encoding and kernel dispatch.  No allocation, no sync on the
+// compute entry points.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "sage_gb300.h"
+#include "sage_internal.h"
+
+namespace sage {
+
+// Device status words, one copy per device that loads the library.
+__device__ int g_status_words[kStatusWords];
+
+namespace {
+
+int* g_status_ptr[64] = {};
+std::mutex g_mu;
+thread_local int g_last_launches = 0;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!tried) {
+        tried = true;
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 3-D tiled map over a [z][y][x] array with a 128-byte swizzled box.
+bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, void* base, uint64_t x, uint64_t y, uint64_t z,
+               uint64_t stride_y_bytes, uint64_t stride_z_bytes, uint32_t box_x, uint32_t box_y) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {x, y, z};
+    cuuint64_t strides[2] = {stride_y_bytes, stride_z_bytes};
+    cuuint32_t box[3] = {box_x, box_y, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, dt, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int check_shape(int B, int H, int Nq, int Nkv, int D) {
+    if (B <= 0 || H <= 0 || Nq <= 0 || Nkv <= 0) return SAGE_ERR_ARG;
+    if (B > 65535 || H > 65535 || Nq > (1 << 24) || Nkv > (1 << 24)) return SAGE_ERR_ARG;
+    if (D != kD) return SAGE_ERR_UNSUPPORTED;
+    return SAGE_OK;
+}
+
+int check_tensor(const sage_tensor* t) {
+    if (t == nullptr || t->ptr == nullptr) return SAGE_ERR_ARG;
+    if (!aligned16(t->ptr)) return SAGE_ERR_UNSUPPORTED;
+    if ((t->stride_b % 8) || (t->stride_h % 8) || (t->stride_n % 8)) return SAGE_ERR_UNSUPPORTED;
+    if (t->stride_b < 0 || t->stride_h < 0 || t->stride_n < 0) return SAGE_ERR_UNSUPPORTED;
+    return SAGE_OK;
+}
+
+int check_prep_buffers(const sage_prep_buffers* p, bool need_workspace, const sage_sizes& sz) {
+    if (p == nullptr) return SAGE_ERR_ARG;
+    if (!p->q16 || !p->k16 || !p->v8t || !p->q_scale || !p->k_scale || !p->v_scale || !p->k_mean)
+        return SAGE_ERR_ARG;
+    const void* ptrs[] = {p->q16, p->k16, p->v8t, p->q_scale, p->k_scale, p->v_scale, p->k_mean};
+    for (const void* q : ptrs)
+        if (!aligned16(q)) return SAGE_ERR_UNSUPPORTED;
+    if ((p->q8 && !aligned16(p->q8)) || (p->k8 && !aligned16(p->k8))) return SAGE_ERR_UNSUPPORTED;
+    if (need_workspace) {
+        if (!p->workspace || !aligned16(p->workspace)) return SAGE_ERR_ARG;
+        if (p->workspace_bytes < sz.workspace) return SAGE_ERR_ARG;
+    }
+    return SAGE_OK;
+}
+
+int status_from(cudaError_t e) { return e == cudaSuccess ? SAGE_OK : SAGE_ERR_LAUNCH; }
+
+int fault_mode_for_next_launch = 0;
+
+}  // namespace
+
+int* device_status_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_status_ptr[dev] == nullptr) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_status_words) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<int*>(ptr);
+    }
+    return g_status_ptr[dev];
+}
+
+}  // namespace sage
+
+using namespace sage;
+
+extern "C" {
+
+int sage_buffer_sizes(int B, int H, int Nq, int Nkv, int D, sage_sizes* out) {
+    if (out == nullptr) return SAGE_ERR_ARG;
+    const int rc = check_shape(B, H, Nq, Nkv, D);
+    if (rc != SAGE_OK) return rc;
+    const int64_t bh = (int64_t)B * H;
+    const int64_t pad = nkv_pad_of(Nkv);
+    const int64_t nchunks = ceil_div(Nkv, kMeanChunk);
+    out->q16 = (size_t)(bh * Nq * kD * 2);
+    out->k16 = (size_t)(bh * Nkv * kD * 2);
+    out->v8t = (size_t)(bh * kD * pad);
+    out->q_scale = (size_t)(bh * ceil_div(Nq, kBQS) * 4);
+    out->k_scale = (size_t)(bh * ceil_div(Nkv, kBKS) * 4);
+    out->v_scale = (size_t)(bh * kD * 4);
+    out->k_mean = (size_t)(bh * kD * 4);
+    out->q8 = (size_t)(bh * Nq * kD);
+    out->k8 = (size_t)(bh * Nkv * kD);
+    // partial sums + partial amax [B,H,chunks,D] and the V inverse scales [B,H,D]
+    out->workspace = (size_t)(2 * bh * nchunks * kD * 4 + bh * kD * 4);
+    out->nkv_pad = pad;
+    return SAGE_OK;
+}
+
+int sage_prep_qkv(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v, int B, int H, int Nq,
+                  int Nkv, int D, const int32_t* q_len, const int32_t* kv_len, const sage_prep_buffers* out,
+                  void* stream) {
+    int rc = check_shape(B, H, Nq, Nkv, D);
+    if (rc != SAGE_OK) return rc;
+    if ((rc = check_tensor(q)) != SAGE_OK || (rc = check_tensor(k)) != SAGE_OK || (rc = check_tensor(v)) != SAGE_OK)
+        return rc;
+    sage_sizes sz;
+    sage_buffer_sizes(B, H, Nq, Nkv, D, &sz);
+    if ((rc = check_prep_buffers(out, true, sz)) != SAGE_OK) return rc;
+
+    PrepParams p{};
+    p.q = static_cast<const uint16_t*>(q->ptr);
+    p.k = static_cast<const uint16_t*>(k->ptr);
+    p.v = static_cast<const uint16_t*>(v->ptr);
+    p.qsb = q->stride_b; p.qsh = q->stride_h; p.qsn = q->stride_n;
+    p.ksb = k->stride_b; p.ksh = k->stride_h; p.ksn = k->stride_n;
+    p.vsb = v->stride_b; p.vsh = v->stride_h; p.vsn = v->stride_n;
+    p.B = B; p.H = H; p.Nq = Nq; p.Nkv = Nkv;
+    p.nkv_pad = (int)sz.nkv_pad;
+    p.nq_blocks = (int)ceil_div(Nq, kBQS);
+    p.nk_blocks = (int)ceil_div(Nkv, kBKS);
+    p.n_chunks = (int)ceil_div(Nkv, kMeanChunk);
+    p.q_len = q_len; p.kv_len = kv_len;
+    p.q16 = out->q16; p.k16 = out->k16; p.v8t = out->v8t;
+    p.q8 = out->q8; p.k8 = out->k8;
+    p.q_scale = out->q_scale; p.k_scale = out->k_scale; p.v_scale = out->v_scale; p.k_mean = out->k_mean;
+    float* ws = static_cast<float*>(out->workspace);
+    const int64_t part = (int64_t)B * H * p.n_chunks * kD;
+    p.psum = ws;
+    p.pamax = ws + part;
+    p.v_inv = ws + 2 * part;
+    int launches = 0;
+    rc = status_from(launch_prep(p, static_cast<cudaStream_t>(stream), &launches));
+    if (rc == SAGE_OK) g_last_launches = launches;
+    return rc;
+}
+
+static int attn_common(const sage_prep_buffers* in, const sage_tensor* o, int32_t* s_out, int B, int H, int Nq,
+                       int Nkv, int D, const int32_t* q_len, const int32_t* kv_len, float sm_scale,
+                       void* stream, bool capture) {
+    int rc = check_shape(B, H, Nq, Nkv, D);
+    if (rc != SAGE_OK) return rc;
+    sage_sizes sz;
+    sage_buffer_sizes(B, H, Nq, Nkv, D, &sz);
+    if ((rc = check_prep_buffers(in, false, sz)) != SAGE_OK) return rc;
+    if (capture) {
+        if (s_out == nullptr) return SAGE_ERR_ARG;
+    } else if ((rc = check_tensor(o)) != SAGE_OK) {
+        return rc;
+    }
+    int* status = device_status_ptr();
+    if (status == nullptr) return SAGE_ERR_LAUNCH;
+
+    const uint64_t bh = (uint64_t)B * H;
+    CUtensorMap tq, tk, tv;
+    if (!encode_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, in->q16, kD, (uint64_t)Nq, bh, kD * 2,
+                   (uint64_t)Nq * kD * 2, 64, 128) ||
+        !encode_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, in->k16, kD, (uint64_t)Nkv, bh, kD * 2,
+                   (uint64_t)Nkv * kD * 2, 64, 128) ||
+        !encode_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, in->v8t, (uint64_t)sz.nkv_pad, kD, bh,
+                   (uint64_t)sz.nkv_pad, (uint64_t)sz.nkv_pad * kD, 128, 128))
+        return encode_fn() ? SAGE_ERR_UNSUPPORTED : SAGE_ERR_DRIVER;
+
+    AttnParams p{};
+    p.q_scale = in->q_scale; p.k_scale = in->k_scale; p.v_scale = in->v_scale;
+    p.q_len = q_len; p.kv_len = kv_len;
+    if (!capture) {
+        p.o = static_cast<uint16_t*>(const_cast<void*>(o->ptr));
+        p.osb = o->stride_b; p.osh = o->stride_h; p.osn = o->stride_n;
+    }
+    p.s_out = s_out;
+    p.B = B; p.H = H; p.Nq = Nq; p.Nkv = Nkv;
+    p.nq_blocks = (int)ceil_div(Nq, kBQS);
+    p.nk_blocks = (int)ceil_div(Nkv, kBKS);
+    const double scale = sm_scale > 0.f ? (double)sm_scale : 1.0 / std::sqrt((double)D);
+    p.c = (float)(scale * (1.0 / std::log(2.0)));
+    p.status = status;
+    p.fault_mode = fault_mode_for_next_launch;
+    fault_mode_for_next_launch = 0;
+    int launches = 0;
+    rc = status_from(launch_attn(p, tq, tk, tv, capture, static_cast<cudaStream_t>(stream), &launches));
+    if (rc == SAGE_OK) g_last_launches = launches;
+    return rc;
+}
+
+int sage_attn_fwd(const sage_prep_buffers* in, const sage_tensor* o, int B, int H, int Nq, int Nkv, int D,
+                  const int32_t* q_len, const int32_t* kv_len, float sm_scale, void* stream) {
+    return attn_common(in, o, nullptr, B, H, Nq, Nkv, D, q_len, kv_len, sm_scale, stream, false);
+}
+
+int sage_qk_int32(const sage_prep_buffers* in, int32_t* s, int B, int H, int Nq, int Nkv, int D,
+                  const int32_t* q_len, const int32_t* kv_len, void* stream) {
+    return attn_common(in, nullptr, s, B, H, Nq, Nkv, D, q_len, kv_len, 0.f, stream, true);
+}
+
+int sage_attention_host(const sage_copy* inputs, int n_inputs, const sage_tensor* q, const sage_tensor* k,
+                        const sage_tensor* v, const sage_prep_buffers* buf, const sage_tensor* o,
+                        const sage_copy* output, int B, int H, int Nq, int Nkv, int D, float sm_scale,
+                        void* stream) {
+    if (inputs == nullptr || n_inputs <= 0 || output == nullptr) return SAGE_ERR_ARG;
+    int rc = check_shape(B, H, Nq, Nkv, D);
+    if (rc != SAGE_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    for (int i = 0; i < n_inputs; ++i) {
+        if (!inputs[i].host || !inputs[i].device) return SAGE_ERR_ARG;
+        if (cudaMemcpyAsync(inputs[i].device, inputs[i].host, inputs[i].bytes, cudaMemcpyHostToDevice, s) !=
+            cudaSuccess)
+            return SAGE_ERR_LAUNCH;
+    }
+    rc = sage_prep_qkv(q, k, v, B, H, Nq, Nkv, D, nullptr, nullptr, buf, stream);
+    if (rc != SAGE_OK) return rc;
+    const int prep_launches = g_last_launches;
+    rc = sage_attn_fwd(buf, o, B, H, Nq, Nkv, D, nullptr, nullptr, sm_scale, stream);
+    if (rc != SAGE_OK) return rc;
+    g_last_launches += prep_launches;
+    if (!output->host || !output->device) return SAGE_ERR_ARG;
+    if (cudaMemcpyAsync(const_cast<void*>(output->host), output->device, output->bytes, cudaMemcpyDeviceToHost,
+                        s) != cudaSuccess)
+        return SAGE_ERR_LAUNCH;
+    return SAGE_OK;
+}
+
+int sage_get_device_status(void) {
+    int* st = device_status_ptr();
+    if (st == nullptr) return SAGE_ERR_LAUNCH;
+    if (cudaDeviceSynchronize() != cudaSuccess) return SAGE_ERR_LAUNCH;
+    int words[kStatusWords] = {0, 0, 0, 0};
+    if (cudaMemcpy(words, st, sizeof(words), cudaMemcpyDeviceToHost) != cudaSuccess) return SAGE_ERR_LAUNCH;
+    const int zero[kStatusWords] = {0, 0, 0, 0};
+    if (cudaMemcpy(st, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return SAGE_ERR_LAUNCH;
+    return words[0];
+}
+
+const char* sage_status_string(int code) {
+    switch (code) {
+        case SAGE_OK: return "ok";
+        case SAGE_ERR_ARG: return "invalid argument";
+        case SAGE_ERR_UNSUPPORTED: return "unsupported shape, alignment or stride";
+        case SAGE_ERR_LAUNCH: return "CUDA launch error";
+        case SAGE_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
+        case SAGE_ERR_DRIVER: return "driver entry point cuTensorMapEncodeTiled unavailable";
+        default: return "unknown status";
+    }
+}
+
+int sage_last_launch_count(void) { return g_last_launches; }
+
+// Test hook (not part of the public header): the next sage_attn_fwd launch
+// withholds one V tile copy so its consumer's bounded wait runs out.
+int sage_debug_inject_fault(int mode) {
+    fault_mode_for_next_launch = mode;
+    return SAGE_OK;
+}
+
+}  // extern "C"

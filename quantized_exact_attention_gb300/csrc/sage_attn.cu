@@ -1,0 +1,514 @@
+// sage_attn.cu - fused quantized attention for sm_103a.
+//
+// One CTA computes one 128-row query tile of one (b, h) head.  It follows the
+// numerical contract's stage order (Experiment Log, "Phase 0 Import And
+// Verification": QK traversal, online softmax, FP8 V/P, two-level PV
+// accumulation, final conversion, ragged tails) with the state split that
+// "Phase 1 State-Ownership Decision" argues for: QK/softmax state and
+// PV/output state live in different warps, and every KV tile is processed in
+// strict order with a per-tile rescale of the FP32 running output (RO).
+//
+// Warp roles (320 threads):
+//   warps 0-3  softmax: thread r owns query row r; reads S from tensor memory,
+//              row max, alpha = 2^(m_old - m_new), p = 2^(S*f - m_new),
+//              row sum, e4m3 packing of P into tensor memory
+//   warps 4-7  correction: thread r owns RO[r, 0:128] in registers; per tile
+//              RO = RO * alpha + fp16(PV); epilogue 1/l, V scale, BF16 store
+//   warp 8     TMA producer: Q once, then K (FP16 integer codes) and V (e4m3,
+//              token-fastest) tiles through 3-deep rings
+//   warp 9     tensor-memory allocator and single-thread tcgen05 issuer:
+//              S_t = Q K_t^T (kind::f16, exact for INT8 codes: |sum| < 2^21
+//              < 2^24) and PV_t = P_t V_t (kind::f8f6f4, P read from tensor
+//              memory)
+//
+// Tensor memory (512 columns x 128 lanes): S double buffer [0,256), PV
+// [256,384), P double buffer [384,448) (4 e4m3 values per 32-bit column).
+//
+// Every mbarrier wait is bounded (sage_ptx.cuh); a wait that runs out records
+// SAGE_ERR_TIMEOUT in the device status words, raises a CTA-wide abort flag,
+// lets the other roles leave their loops, drains the copies and MMAs in
+// flight, frees tensor memory and returns.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "sage_internal.h"
+#include "sage_ptx.cuh"
+
+namespace sage {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kNK = 3;              // K ring depth
+constexpr int kNV = 3;              // V ring depth
+constexpr uint32_t kTileQBytes = 128 * 128 * 2;
+constexpr uint32_t kTileKBytes = 128 * 128 * 2;
+constexpr uint32_t kTileVBytes = 128 * 128;
+constexpr uint32_t kHalfBytes = 128 * 128;      // one 64-column half of an FP16 tile
+
+// shared memory map (offsets from a 1024-byte aligned base)
+constexpr uint32_t OFF_Q = 0;
+constexpr uint32_t OFF_K = OFF_Q + kTileQBytes;
+constexpr uint32_t OFF_V = OFF_K + kNK * kTileKBytes;
+constexpr uint32_t OFF_BAR = OFF_V + kNV * kTileVBytes;
+
+enum Bar : uint32_t {
+    B_QFULL = 0,
+    B_KFULL = 1,
+    B_KEMPTY = B_KFULL + kNK,
+    B_VFULL = B_KEMPTY + kNK,
+    B_VEMPTY = B_VFULL + kNV,
+    B_SFULL = B_VEMPTY + kNV,
+    B_SFREE = B_SFULL + 2,
+    B_PFULL = B_SFREE + 2,
+    B_PFREE = B_PFULL + 2,
+    B_PVFULL = B_PFREE + 2,
+    B_PVFREE = B_PVFULL + 1,
+    B_AFULL = B_PVFREE + 1,
+    B_AFREE = B_AFULL + 2,
+    B_LFULL = B_AFREE + 2,
+    B_DRAIN = B_LFULL + 1,
+    B_COUNT = B_DRAIN + 1
+};
+
+constexpr uint32_t OFF_ALPHA = OFF_BAR + ((B_COUNT * 8 + 15) / 16) * 16;   // float [2][128]
+constexpr uint32_t OFF_L = OFF_ALPHA + 2 * 128 * 4;                        // float [128]
+constexpr uint32_t OFF_VS = OFF_L + 128 * 4;                               // float [128]
+constexpr uint32_t OFF_TMEM = OFF_VS + 128 * 4;                            // u32
+constexpr uint32_t OFF_ABORT = OFF_TMEM + 16;                              // int
+constexpr uint32_t kSmemUsed = OFF_ABORT + 16;
+constexpr uint32_t kSmemBytes = kSmemUsed + 1024;                          // + alignment slack
+
+constexpr uint32_t TM_S = 0;        // S buffer b at column 128*b
+constexpr uint32_t TM_PV = 256;
+constexpr uint32_t TM_P = 384;      // P buffer b at column 384 + 32*b
+constexpr uint32_t kTmemCols = 512;
+
+constexpr float kLog2SP = 8.807354922057604f;   // log2(448)
+
+enum Role { R_SOFTMAX = 1, R_CORRECT = 2, R_PRODUCER = 3, R_MMA = 4 };
+
+__device__ __forceinline__ int clamp_len(const int32_t* lens, int b, int n) {
+    if (lens == nullptr) return n;
+    int v = lens[b];
+    return v < 0 ? 0 : (v > n ? n : v);
+}
+
+__device__ __forceinline__ void record_failure(const AttnParams& p, volatile int* abort_flag, int role, int tile) {
+    *abort_flag = 1;
+    if (atomicCAS(p.status, 0, -4 /* SAGE_ERR_TIMEOUT */) == 0) {
+        p.status[1] = (int)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
+        p.status[2] = role;
+        p.status[3] = tile;
+    }
+}
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
+    const bool ok = mbar_wait(bar, parity, abort_flag);
+    return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+    return lo | (hi << 16);
+}
+
+__device__ __forceinline__ float fp16_round(float x) {
+    return __half2float(__float2half_rn(x));
+}
+
+template <bool kCapture>
+__global__ void __launch_bounds__(kThreads, 1)
+sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_base = smem_u32(smem_raw);
+    const uint32_t sbase = (raw_base + 1023u) & ~1023u;
+    uint8_t* sgen = smem_raw + (sbase - raw_base);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int qtile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int bh = b * p.H + h;
+    const int q0 = qtile * 128;
+    const int lq = clamp_len(p.q_len, b, p.Nq);
+    const int lk = clamp_len(p.kv_len, b, p.Nkv);
+    if (q0 >= lq) return;                                   // no valid row in this tile
+
+    if (lk == 0) {                                          // no keys: rows are zero
+        if (!kCapture && threadIdx.x < 128) {
+            const int r = q0 + threadIdx.x;
+            if (r < lq) {
+                uint4* dst = reinterpret_cast<uint4*>(p.o + b * p.osb + h * p.osh + (int64_t)r * p.osn);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+            }
+        }
+        return;
+    }
+    const int T = (lk + 127) / 128;                         // KV tiles
+
+    auto bar = [&](uint32_t i) -> uint32_t { return sbase + OFF_BAR + 8u * i; };
+    float* alpha_s = reinterpret_cast<float*>(sgen + OFF_ALPHA);
+    float* l_s = reinterpret_cast<float*>(sgen + OFF_L);
+    float* vs_s = reinterpret_cast<float*>(sgen + OFF_VS);
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sgen + OFF_TMEM);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + OFF_ABORT);
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        mbar_init(bar(B_QFULL), 1);
+        for (int i = 0; i < kNK; ++i) { mbar_init(bar(B_KFULL + i), 1); mbar_init(bar(B_KEMPTY + i), 1); }
+        for (int i = 0; i < kNV; ++i) { mbar_init(bar(B_VFULL + i), 1); mbar_init(bar(B_VEMPTY + i), 1); }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(B_SFULL + i), 1);
+            mbar_init(bar(B_SFREE + i), 128);
+            mbar_init(bar(B_PFULL + i), 128);
+            mbar_init(bar(B_PFREE + i), 1);
+            mbar_init(bar(B_AFULL + i), 128);
+            mbar_init(bar(B_AFREE + i), 128);
+        }
+        mbar_init(bar(B_PVFULL), 1);
+        mbar_init(bar(B_PVFREE), 128);
+        mbar_init(bar(B_LFULL), 128);
+        mbar_init(bar(B_DRAIN), 1);
+        fence_mbar_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(sbase + OFF_TMEM, kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 8 && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        if (!kCapture) tma_prefetch_desc(&tm_v);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp < 4) {
+        // ===================================================== softmax
+        const int row = threadIdx.x;
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const float qs = p.q_scale[(int64_t)bh * p.nq_blocks + qtile];
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int t = 0; t < T; ++t) {
+            const int sb = t & 1;
+            const int kb0 = 2 * t, kb1 = 2 * t + 1;
+            const float ks0 = (kb0 * 64 < lk) ? p.k_scale[(int64_t)bh * p.nk_blocks + kb0] : 0.f;
+            const float ks1 = (kb1 * 64 < lk) ? p.k_scale[(int64_t)bh * p.nk_blocks + kb1] : 0.f;
+            const float f0 = __fmul_rn(__fmul_rn(qs, ks0), p.c);
+            const float f1 = __fmul_rn(__fmul_rn(qs, ks1), p.c);
+            if (!warp_wait(bar(B_SFULL + sb), (t >> 1) & 1, abort_flag)) {
+                if (lane == 0) record_failure(p, abort_flag, R_SOFTMAX, t);
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t s[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_base + TM_S + sb * 128 + c * 32, s[c]);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(bar(B_SFREE + sb));
+
+            const int valid = lk - t * 128;                 // >= 1 valid key in this tile
+            if (kCapture) {
+                const int r = q0 + row;
+                if (r < lq) {
+                    int32_t* dst = p.s_out + ((int64_t)bh * p.Nq + r) * p.Nkv + t * 128;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (c * 32 + i < valid) dst[c * 32 + i] = (int32_t)__uint_as_float(s[c][i]);
+                }
+                continue;
+            }
+
+            // row maximum of the raw integer scores per 64-key scale block
+            float mx0, mx1;
+            if (valid >= 128) {
+                float a0 = -INFINITY, a1 = -INFINITY, c0 = -INFINITY, c1 = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    a0 = fmax3(a0, __uint_as_float(s[0][i]), __uint_as_float(s[0][i + 1]));
+                    a1 = fmax3(a1, __uint_as_float(s[1][i]), __uint_as_float(s[1][i + 1]));
+                    c0 = fmax3(c0, __uint_as_float(s[2][i]), __uint_as_float(s[2][i + 1]));
+                    c1 = fmax3(c1, __uint_as_float(s[3][i]), __uint_as_float(s[3][i + 1]));
+                }
+                mx0 = fmaxf(a0, a1);
+                mx1 = fmaxf(c0, c1);
+            } else {
+                mx0 = -INFINITY;
+                mx1 = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int col = c * 32 + i;
+                        const float v = (col < valid) ? __uint_as_float(s[c][i]) : -INFINITY;
+                        if (c < 2) mx0 = fmaxf(mx0, v); else mx1 = fmaxf(mx1, v);
+                    }
+            }
+            // max of the scaled scores: scaling by f >= 0 is monotone in every rounding
+            const float mt0 = (mx0 == -INFINITY) ? -INFINITY : __fmul_rn(mx0, f0);
+            const float mt1 = (mx1 == -INFINITY) ? -INFINITY : __fmul_rn(mx1, f1);
+            const float m_new = fmaxf(m_run, fmaxf(mt0, mt1));
+            const float alpha = ex2_approx(m_run - m_new);  // first tile: 2^-inf = 0
+            const float nb = kLog2SP - m_new;               // P is produced pre-scaled by 448
+
+            uint32_t pk[32];
+            float ts0 = 0.f, ts1 = 0.f, ts2 = 0.f, ts3 = 0.f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float f = (c < 2) ? f0 : f1;
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    const int col = c * 32 + i;
+                    float e0 = ex2_approx(fmaf(__uint_as_float(s[c][i + 0]), f, nb));
+                    float e1 = ex2_approx(fmaf(__uint_as_float(s[c][i + 1]), f, nb));
+                    float e2 = ex2_approx(fmaf(__uint_as_float(s[c][i + 2]), f, nb));
+                    float e3 = ex2_approx(fmaf(__uint_as_float(s[c][i + 3]), f, nb));
+                    if (valid < 128) {
+                        e0 = (col + 0 < valid) ? e0 : 0.f;
+                        e1 = (col + 1 < valid) ? e1 : 0.f;
+                        e2 = (col + 2 < valid) ? e2 : 0.f;
+                        e3 = (col + 3 < valid) ? e3 : 0.f;
+                    }
+                    ts0 += e0; ts1 += e1; ts2 += e2; ts3 += e3;
+                    pk[col >> 2] = pack_e4m3x4(e0, e1, e2, e3);
+                }
+            }
+            const float tile_sum = (ts0 + ts1) + (ts2 + ts3);
+
+            if (t >= 2 && !warp_wait(bar(B_PFREE + sb), ((t >> 1) - 1) & 1, abort_flag)) {
+                if (lane == 0) record_failure(p, abort_flag, R_SOFTMAX, t);
+                ok = false;
+                break;
+            }
+            tmem_st32(tmem + lane_base + TM_P + sb * 32, pk);
+            tmem_wait_st();
+            if (t >= 2 && !warp_wait(bar(B_AFREE + sb), ((t >> 1) - 1) & 1, abort_flag)) {
+                if (lane == 0) record_failure(p, abort_flag, R_SOFTMAX, t);
+                ok = false;
+                break;
+            }
+            alpha_s[sb * 128 + row] = alpha;
+            tc_fence_before();
+            mbar_arrive(bar(B_PFULL + sb));
+            mbar_arrive(bar(B_AFULL + sb));
+            l_run = fmaf(l_run, alpha, tile_sum);
+            m_run = m_new;
+        }
+        if (!kCapture && ok) {
+            l_s[row] = l_run;
+            mbar_arrive(bar(B_LFULL));
+        }
+    } else if (warp < 8) {
+        // ===================================================== correction + epilogue
+        if (!kCapture) {
+            const int row = threadIdx.x - 128;
+            const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
+            vs_s[row] = p.v_scale[(int64_t)bh * kD + row];
+            named_bar_sync(1, 128);
+            float ro[128];
+#pragma unroll
+            for (int i = 0; i < 128; ++i) ro[i] = 0.f;
+            bool ok = true;
+            for (int t = 0; t < T; ++t) {
+                const int sb = t & 1;
+                if (!warp_wait(bar(B_AFULL + sb), (t >> 1) & 1, abort_flag)) {
+                    if (lane == 0) record_failure(p, abort_flag, R_CORRECT, t);
+                    ok = false;
+                    break;
+                }
+                const float alpha = alpha_s[sb * 128 + row];
+                mbar_arrive(bar(B_AFREE + sb));
+                if (!warp_wait(bar(B_PVFULL), t & 1, abort_flag)) {
+                    if (lane == 0) record_failure(p, abort_flag, R_CORRECT, t);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + lane_base + TM_PV + c * 32, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        ro[c * 32 + i] = fmaf(ro[c * 32 + i], alpha, fp16_round(__uint_as_float(v[i])));
+                }
+                tc_fence_before();
+                mbar_arrive(bar(B_PVFREE));
+            }
+            if (ok && warp_wait(bar(B_LFULL), 0, abort_flag)) {
+                const float rl = __frcp_rn(l_s[row]);     // l carries the 448 scale of P
+                const int r = q0 + row;
+                if (r < lq) {
+                    uint4* dst = reinterpret_cast<uint4*>(p.o + b * p.osb + h * p.osh + (int64_t)r * p.osn);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int d = i * 8 + j * 2;
+                            const float o0 = __fmul_rn(__fmul_rn(ro[d], rl), vs_s[d]);
+                            const float o1 = __fmul_rn(__fmul_rn(ro[d + 1], rl), vs_s[d + 1]);
+                            const __nv_bfloat162 pr = __floats2bfloat162_rn(o0, o1);
+                            w[j] = *reinterpret_cast<const uint32_t*>(&pr);
+                        }
+                        dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+            } else if (ok) {
+                if (lane == 0) record_failure(p, abort_flag, R_CORRECT, T);
+            }
+        }
+    } else if (warp == 8) {
+        // ===================================================== TMA producer
+        if (lane == 0) {
+            const uint32_t sQ = sbase + OFF_Q;
+            int last_k[kNK], last_v[kNV];
+            for (int i = 0; i < kNK; ++i) last_k[i] = -1;
+            for (int i = 0; i < kNV; ++i) last_v[i] = -1;
+            bool ok = true;
+            mbar_arrive_expect_tx(bar(B_QFULL), kTileQBytes);
+            tma_load_3d(sQ, &tm_q, 0, q0, bh, bar(B_QFULL));
+            tma_load_3d(sQ + kHalfBytes, &tm_q, 64, q0, bh, bar(B_QFULL));
+            auto load_k = [&](int t) -> bool {
+                const int st = t % kNK;
+                if (t >= kNK && !mbar_wait(bar(B_KEMPTY + st), ((t / kNK) - 1) & 1, abort_flag)) return false;
+                const uint32_t dst = sbase + OFF_K + st * kTileKBytes;
+                mbar_arrive_expect_tx(bar(B_KFULL + st), kTileKBytes);
+                tma_load_3d(dst, &tm_k, 0, t * 128, bh, bar(B_KFULL + st));
+                tma_load_3d(dst + kHalfBytes, &tm_k, 64, t * 128, bh, bar(B_KFULL + st));
+                last_k[st] = t;
+                return true;
+            };
+            auto load_v = [&](int t) -> bool {
+                const int st = t % kNV;
+                if (t >= kNV && !mbar_wait(bar(B_VEMPTY + st), ((t / kNV) - 1) & 1, abort_flag)) return false;
+                const uint32_t dst = sbase + OFF_V + st * kTileVBytes;
+                mbar_arrive_expect_tx(bar(B_VFULL + st), kTileVBytes);
+                if (p.fault_mode != 1) tma_load_3d(dst, &tm_v, t * 128, 0, bh, bar(B_VFULL + st));
+                last_v[st] = t;
+                return true;
+            };
+            for (int t = 0; t < T && ok; ++t) {
+                ok = load_k(t);
+                if (ok && !kCapture && t >= 1) ok = load_v(t - 1);
+                if (!ok) record_failure(p, abort_flag, R_PRODUCER, t);
+            }
+            if (ok && !kCapture) {
+                ok = load_v(T - 1);
+                if (!ok) record_failure(p, abort_flag, R_PRODUCER, T);
+            }
+            // Drain: every copy issued must land before the CTA may exit.
+            const int zero = 0;
+            const volatile int* no_abort = &zero;
+            mbar_wait(bar(B_QFULL), 0, no_abort);
+            for (int i = 0; i < kNK; ++i)
+                if (last_k[i] >= 0) mbar_wait(bar(B_KFULL + i), (last_k[i] / kNK) & 1, no_abort);
+            if (p.fault_mode != 1)
+                for (int i = 0; i < kNV; ++i)
+                    if (last_v[i] >= 0) mbar_wait(bar(B_VFULL + i), (last_v[i] / kNV) & 1, no_abort);
+        }
+    } else {
+        // ===================================================== MMA issuer (warp 9)
+        if (lane == 0) {
+            constexpr uint32_t kIdescQK = idesc_f32acc(0u, 128u, 128u);   // F16 x F16 -> F32
+            constexpr uint32_t kIdescPV = idesc_f32acc(0u, 128u, 128u);   // E4M3 x E4M3 -> F32
+            const uint32_t sQ = sbase + OFF_Q;
+            bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag);
+            int fail_tile = 0;
+            auto issue_qk = [&](int t) -> bool {
+                const int st = t % kNK;
+                const int sb = t & 1;
+                if (!mbar_wait(bar(B_KFULL + st), (t / kNK) & 1, abort_flag)) return false;
+                if (t >= 2 && !mbar_wait(bar(B_SFREE + sb), ((t >> 1) - 1) & 1, abort_flag)) return false;
+                tc_fence_after();
+                const uint32_t sK = sbase + OFF_K + st * kTileKBytes;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+                    mma_f16_ss(tmem + TM_S + sb * 128, sdesc_sw128(sQ + off), sdesc_sw128(sK + off),
+                               kIdescQK, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(bar(B_SFULL + sb));
+                mma_commit(bar(B_KEMPTY + st));
+                return true;
+            };
+            auto issue_pv = [&](int t) -> bool {
+                const int sb = t & 1;
+                const int st = t % kNV;
+                if (!mbar_wait(bar(B_PFULL + sb), (t >> 1) & 1, abort_flag)) return false;
+                if (!mbar_wait(bar(B_VFULL + st), (t / kNV) & 1, abort_flag)) return false;
+                if (t >= 1 && !mbar_wait(bar(B_PVFREE), (t - 1) & 1, abort_flag)) return false;
+                tc_fence_after();
+                const uint32_t sV = sbase + OFF_V + st * kTileVBytes;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_f8_ts(tmem + TM_PV, tmem + TM_P + sb * 32 + kk * 8, sdesc_sw128(sV + kk * 32),
+                              kIdescPV, kk > 0 ? 1u : 0u);
+                mma_commit(bar(B_PVFULL));
+                mma_commit(bar(B_PFREE + sb));
+                mma_commit(bar(B_VEMPTY + st));
+                return true;
+            };
+            if (ok) ok = issue_qk(0);
+            for (int t = 0; t < T && ok; ++t) {
+                fail_tile = t;
+                if (t + 1 < T) ok = issue_qk(t + 1);
+                if (ok && !kCapture) ok = issue_pv(t);
+            }
+            if (!ok) record_failure(p, abort_flag, R_MMA, fail_tile);
+            // Drain: all MMAs issued by this thread complete before teardown.
+            mma_commit(bar(B_DRAIN));
+            const int zero = 0;
+            mbar_wait(bar(B_DRAIN), 0, &zero);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+bool g_attr_set[2][64] = {};
+
+template <bool kCapture>
+cudaError_t launch_one(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, cudaStream_t s) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!g_attr_set[kCapture ? 1 : 0][dev]) {
+        cudaError_t e = cudaFuncSetAttribute(sage_attn_kernel<kCapture>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        g_attr_set[kCapture ? 1 : 0][dev] = true;
+    }
+    dim3 grid((unsigned)((p.Nq + 127) / 128), (unsigned)p.H, (unsigned)p.B);
+    sage_attn_kernel<kCapture><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                        const CUtensorMap& tv, bool capture, cudaStream_t s, int* launches) {
+    *launches = 1;
+    return capture ? launch_one<true>(p, tq, tk, tv, s) : launch_one<false>(p, tq, tk, tv, s);
+}
+
+}  // namespace sage

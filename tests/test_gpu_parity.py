@@ -1,0 +1,92 @@
+"""GPU path vs the oracle, through the C ABI.
+
+Bit-exact: FP16/INT8 Q and K codes, FP8 V bytes, every scale, the K mean and
+the integer QK scores.  BF16 output: max |diff| <= 1e-2 and relative L2 <=
+5e-3 against the oracle.  The five named workloads run at full size; where the
+oracle would take too long (the 16K-token and the 16x16-head workloads) the
+attention output and the QK scores are compared on sampled query tiles of
+sampled heads, computed by the GPU in the same launch configuration the
+benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import quantized_exact_attention_gb300 as S
+from oracle import sage_oracle as O
+from quantized_exact_attention_gb300 import workloads as W
+from tests import gpu_support as G
+
+pytestmark = pytest.mark.gpu
+
+_CACHE = {}
+
+
+def _run(cfg):
+    if cfg not in _CACHE:
+        _CACHE.clear()
+        torch.cuda.empty_cache()
+        w = W.make_config(cfg)
+        q, k, v = G.logical_f32(w)
+        prep = O.prepare(q, k, v, w.q_len, w.kv_len)
+        run = G.GpuRun(w).prep().attn()
+        _CACHE[cfg] = (w, prep, run)
+    return _CACHE[cfg]
+
+
+def _sample(cfg, w):
+    """(b, h, rows) triples compared against the oracle."""
+    if cfg == 4:
+        tiles = [0, 63, 127]
+        return [(0, h, np.concatenate([np.arange(t * 128, t * 128 + 128) for t in tiles]))
+                for h in (0, 11, 23)]
+    if cfg == 5:
+        return [(b, h, np.arange(w.Nq)) for b, h in ((0, 0), (7, 3), (15, 15))]
+    return [(b, h, np.arange(w.qlens[b])) for b in range(w.B) for h in range(w.H)]
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+def test_prep_bit_exact(cfg):
+    w, prep, run = _run(cfg)
+    G.compare_prep(run, prep)
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+def test_qk_scores_bit_exact(cfg):
+    w, prep, run = _run(cfg)
+    s = run.qk()
+    for b, h, rows in _sample(cfg, w):
+        lk = w.kvlens[b]
+        ref = O.qk_scores(prep.q8[b, h][rows], prep.k8[b, h][:lk])
+        got = s[b, h][torch.as_tensor(rows, device="cuda")][:, :lk].cpu().numpy().astype(np.int64)
+        assert np.array_equal(got, ref), f"b={b} h={h}: {np.count_nonzero(got != ref)} scores differ"
+    del s
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+def test_attention_matches_oracle(cfg):
+    w, prep, run = _run(cfg)
+    out = run.out_bits()                                      # [B, H, Nq, D] bf16 bits
+    worst = (0.0, 0.0)
+    for b, h, rows in _sample(cfg, w):
+        ref, _ = O.attention_rows(prep, b, h, rows)
+        got = out[b, h][rows]
+        ma, rel = G.out_metrics(got, ref)
+        worst = (max(worst[0], ma), max(worst[1], rel))
+        assert ma <= G.OUT_MAX_ABS and rel <= G.OUT_REL_L2, f"b={b} h={h}: max_abs={ma} rel={rel}"
+    # rows beyond a batch item's length were never written
+    for b in range(w.B):
+        assert np.all(out[b, :, w.qlens[b]:] == 0)
+    print(f"cfg{cfg}: worst max_abs={worst[0]:.3e} rel_l2={worst[1]:.3e}")
+
+
+@pytest.mark.parametrize("cfg", [1, 3])
+def test_repeated_launches_are_bit_identical(cfg):
+    w, prep, run = _run(cfg)
+    first = run.out_bits().copy()
+    codes = run.bufs.v8t.clone(), run.bufs.q16.clone(), run.bufs.k16.clone()
+    for _ in range(5):
+        run.prep().attn()
+        assert np.array_equal(run.out_bits(), first)
+    assert all(torch.equal(a, b) for a, b in zip(codes, (run.bufs.v8t, run.bufs.q16, run.bufs.k16)))
