@@ -1,8 +1,8 @@
 """GPU path vs the oracle, through the C ABI.
 
 Bit-exact: FP16/INT8 Q and K codes, FP8 V bytes, every scale, the K mean and
-the integer QK scores.  BF16 output: max |diff| <= 1e-2 and relative L2 <=
-5e-3 against the oracle.  The five named workloads run at full size; where the
+the integer QK scores.  BF16 output: |diff| <= max(1e-2, one BF16 ulp of the
+oracle value) per element and relative L2 <= 5e-3 against the oracle.  The five named workloads run at full size; where the
 oracle would take too long (the 16K-token and the 16x16-head workloads) the
 attention output and the QK scores are compared on sampled query tiles of
 sampled heads, computed by the GPU in the same launch configuration the
@@ -72,9 +72,9 @@ def test_attention_matches_oracle(cfg):
     for b, h, rows in _sample(cfg, w):
         ref, _ = O.attention_rows(prep, b, h, rows)
         got = out[b, h][rows]
-        ma, rel = G.out_metrics(got, ref)
+        ex, rel, ma = G.out_metrics(got, ref)
         worst = (max(worst[0], ma), max(worst[1], rel))
-        assert ma <= G.OUT_MAX_ABS and rel <= G.OUT_REL_L2, f"b={b} h={h}: max_abs={ma} rel={rel}"
+        assert ex <= 0 and rel <= G.OUT_REL_L2, f"b={b} h={h}: max_abs={ma} rel={rel}"
     # rows beyond a batch item's length were never written
     for b in range(w.B):
         assert np.all(out[b, :, w.qlens[b]:] == 0)
