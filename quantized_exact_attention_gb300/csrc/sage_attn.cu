@@ -8,18 +8,22 @@
 // PV/output state live in different warps, and every KV tile is processed in
 // strict order with a per-tile rescale of the FP32 running output (RO).
 //
-// Warp roles (320 threads):
-//   warps 0-3  softmax: thread r owns query row r; reads S from tensor memory,
-//              row max, alpha = 2^(m_old - m_new), p = 2^(S*f - m_new),
-//              row sum, e4m3 packing of P into tensor memory
-//   warps 4-7  correction: thread r owns RO[r, 0:128] in registers; per tile
-//              RO = RO * alpha + fp16(PV); epilogue 1/l, V scale, BF16 store
-//   warp 8     TMA producer: Q once, then K (FP16 integer codes) and V (e4m3,
-//              token-fastest) tiles through 3-deep rings
-//   warp 9     tensor-memory allocator and single-thread tcgen05 issuer:
-//              S_t = Q K_t^T (kind::f16, exact for INT8 codes: |sum| < 2^21
-//              < 2^24) and PV_t = P_t V_t (kind::f8f6f4, P read from tensor
-//              memory)
+// Warp roles (576 threads).  Each query row is split between two threads of
+// two warps that see the same tensor-memory lane quarter: "half" 0 owns key
+// columns 0-63 of every tile (one 64-key K scale block) and output channels
+// 0-63, half 1 owns columns 64-127 and channels 64-127.
+//   warps 0-7   softmax: S from tensor memory, half-row max, exchange of the
+//               two half maxima through shared memory, alpha = 2^(m_old -
+//               m_new), p*448 = 2^(S*f - m_new + log2 448) (packed FP32 pair
+//               FMAs), half-row sums, e4m3 packing of P into tensor memory
+//   warps 8-15  correction: RO[row, 64 channels] in registers; per tile
+//               RO = RN(RN(RO * alpha) + fp16(PV)); epilogue 1/l, V scale, BF16
+//   warp 16     TMA producer: Q once, then K (FP16 integer codes) and V (e4m3,
+//               token-fastest) tiles through 3-deep rings
+//   warp 17     tensor-memory allocator and single-thread tcgen05 issuer:
+//               S_t = Q K_t^T (kind::f16, exact for INT8 codes: |sum| < 2^21
+//               < 2^24) and PV_t = P_t V_t (kind::f8f6f4, P read from tensor
+//               memory)
 //
 // Tensor memory (512 columns x 128 lanes): S double buffer [0,256), PV
 // [256,384), P double buffer [384,448) (4 e4m3 values per 32-bit column).
@@ -38,7 +42,9 @@
 namespace sage {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 576;
+constexpr int kWarpProducer = 16;
+constexpr int kWarpMma = 17;
 constexpr int kNK = 3;              // K ring depth
 constexpr int kNV = 3;              // V ring depth
 constexpr uint32_t kTileQBytes = 128 * 128 * 2;
@@ -72,8 +78,9 @@ enum Bar : uint32_t {
 };
 
 constexpr uint32_t OFF_ALPHA = OFF_BAR + ((B_COUNT * 8 + 15) / 16) * 16;   // float [2][128]
-constexpr uint32_t OFF_L = OFF_ALPHA + 2 * 128 * 4;                        // float [128]
-constexpr uint32_t OFF_VS = OFF_L + 128 * 4;                               // float [128]
+constexpr uint32_t OFF_XM = OFF_ALPHA + 2 * 128 * 4;                       // float [2 buf][2 half][128]
+constexpr uint32_t OFF_L = OFF_XM + 4 * 128 * 4;                           // float [2 half][128]
+constexpr uint32_t OFF_VS = OFF_L + 2 * 128 * 4;                           // float [128]
 constexpr uint32_t OFF_TMEM = OFF_VS + 128 * 4;                            // u32
 constexpr uint32_t OFF_ABORT = OFF_TMEM + 16;                              // int
 constexpr uint32_t kSmemUsed = OFF_ABORT + 16;
@@ -112,10 +119,6 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
     const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
     const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
     return lo | (hi << 16);
-}
-
-__device__ __forceinline__ float fp16_round(float x) {
-    return __half2float(__float2half_rn(x));
 }
 
 template <bool kCapture>
@@ -163,23 +166,23 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         for (int i = 0; i < kNV; ++i) { mbar_init(bar(B_VFULL + i), 1); mbar_init(bar(B_VEMPTY + i), 1); }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B_SFULL + i), 1);
-            mbar_init(bar(B_SFREE + i), 128);
-            mbar_init(bar(B_PFULL + i), 128);
+            mbar_init(bar(B_SFREE + i), 256);     // every softmax thread
+            mbar_init(bar(B_PFULL + i), 256);     // every softmax thread
             mbar_init(bar(B_PFREE + i), 1);
-            mbar_init(bar(B_AFULL + i), 128);
-            mbar_init(bar(B_AFREE + i), 128);
+            mbar_init(bar(B_AFULL + i), 128);     // softmax half 0 (writes alpha)
+            mbar_init(bar(B_AFREE + i), 256);     // every correction thread
         }
         mbar_init(bar(B_PVFULL), 1);
-        mbar_init(bar(B_PVFREE), 128);
-        mbar_init(bar(B_LFULL), 128);
+        mbar_init(bar(B_PVFREE), 256);            // every correction thread
+        mbar_init(bar(B_LFULL), 256);             // every softmax thread
         mbar_init(bar(B_DRAIN), 1);
         fence_mbar_init();
     }
-    if (warp == 9) {
+    if (warp == kWarpMma) {
         tmem_alloc(sbase + OFF_TMEM, kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 8 && lane == 0) {
+    if (warp == kWarpProducer && lane == 0) {
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         if (!kCapture) tma_prefetch_desc(&tm_v);
@@ -189,136 +192,138 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp < 4) {
+    if (warp < 8) {
         // ===================================================== softmax
-        const int row = threadIdx.x;
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const int quarter = warp & 3, half = warp >> 2;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        float* xm = reinterpret_cast<float*>(sgen + OFF_XM);    // [buf][half][row]
         const float qs = p.q_scale[(int64_t)bh * p.nq_blocks + qtile];
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         for (int t = 0; t < T; ++t) {
             const int sb = t & 1;
-            const int kb0 = 2 * t, kb1 = 2 * t + 1;
-            const float ks0 = (kb0 * 64 < lk) ? p.k_scale[(int64_t)bh * p.nk_blocks + kb0] : 0.f;
-            const float ks1 = (kb1 * 64 < lk) ? p.k_scale[(int64_t)bh * p.nk_blocks + kb1] : 0.f;
-            const float f0 = __fmul_rn(__fmul_rn(qs, ks0), p.c);
-            const float f1 = __fmul_rn(__fmul_rn(qs, ks1), p.c);
+            const int kb = 2 * t + half;                    // this half's 64-key scale block
+            const float ks = (kb * 64 < lk) ? p.k_scale[(int64_t)bh * p.nk_blocks + kb] : 0.f;
+            const float f = __fmul_rn(__fmul_rn(qs, ks), p.c);
             if (!warp_wait(bar(B_SFULL + sb), (t >> 1) & 1, abort_flag)) {
                 if (lane == 0) record_failure(p, abort_flag, R_SOFTMAX, t);
                 ok = false;
                 break;
             }
             tc_fence_after();
-            uint32_t s[4][32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_base + TM_S + sb * 128 + c * 32, s[c]);
+            uint32_t s0[32], s1[32];
+            tmem_ld32(tmem + lane_base + TM_S + sb * 128 + half * 64, s0);
+            tmem_ld32(tmem + lane_base + TM_S + sb * 128 + half * 64 + 32, s1);
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(bar(B_SFREE + sb));
+            const int lim = lk - t * 128 - half * 64;       // valid columns of this half (may be <= 0)
 
-            const int valid = lk - t * 128;                 // >= 1 valid key in this tile
             if (kCapture) {
                 const int r = q0 + row;
                 if (r < lq) {
-                    int32_t* dst = p.s_out + ((int64_t)bh * p.Nq + r) * p.Nkv + t * 128;
+                    int32_t* dst = p.s_out + ((int64_t)bh * p.Nq + r) * p.Nkv + t * 128 + half * 64;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (c * 32 + i < valid) dst[c * 32 + i] = (int32_t)__uint_as_float(s[c][i]);
+                    for (int i = 0; i < 32; ++i) {
+                        if (i < lim) dst[i] = (int32_t)__uint_as_float(s0[i]);
+                        if (i + 32 < lim) dst[i + 32] = (int32_t)__uint_as_float(s1[i]);
+                    }
                 }
                 continue;
             }
 
-            // row maximum of the raw integer scores per 64-key scale block
-            float mx0, mx1;
-            if (valid >= 128) {
-                float a0 = -INFINITY, a1 = -INFINITY, c0 = -INFINITY, c1 = -INFINITY;
+            // half-row maximum of the raw integer scores
+            float mx;
+            if (lim >= 64) {
+                float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    a0 = fmax3(a0, __uint_as_float(s[0][i]), __uint_as_float(s[0][i + 1]));
-                    a1 = fmax3(a1, __uint_as_float(s[1][i]), __uint_as_float(s[1][i + 1]));
-                    c0 = fmax3(c0, __uint_as_float(s[2][i]), __uint_as_float(s[2][i + 1]));
-                    c1 = fmax3(c1, __uint_as_float(s[3][i]), __uint_as_float(s[3][i + 1]));
+                for (int i = 0; i < 32; i += 4) {
+                    a0 = fmax3(a0, __uint_as_float(s0[i]), __uint_as_float(s0[i + 1]));
+                    a1 = fmax3(a1, __uint_as_float(s0[i + 2]), __uint_as_float(s0[i + 3]));
+                    a2 = fmax3(a2, __uint_as_float(s1[i]), __uint_as_float(s1[i + 1]));
+                    a3 = fmax3(a3, __uint_as_float(s1[i + 2]), __uint_as_float(s1[i + 3]));
                 }
-                mx0 = fmaxf(a0, a1);
-                mx1 = fmaxf(c0, c1);
+                mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
             } else {
-                mx0 = -INFINITY;
-                mx1 = -INFINITY;
+                mx = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int col = c * 32 + i;
-                        const float v = (col < valid) ? __uint_as_float(s[c][i]) : -INFINITY;
-                        if (c < 2) mx0 = fmaxf(mx0, v); else mx1 = fmaxf(mx1, v);
-                    }
+                for (int i = 0; i < 32; ++i) {
+                    if (i < lim) mx = fmaxf(mx, __uint_as_float(s0[i]));
+                    if (i + 32 < lim) mx = fmaxf(mx, __uint_as_float(s1[i]));
+                }
             }
-            // max of the scaled scores: scaling by f >= 0 is monotone in every rounding
-            const float mt0 = (mx0 == -INFINITY) ? -INFINITY : __fmul_rn(mx0, f0);
-            const float mt1 = (mx1 == -INFINITY) ? -INFINITY : __fmul_rn(mx1, f1);
-            const float m_new = fmaxf(m_run, fmaxf(mt0, mt1));
+            // scaling by f >= 0 is monotone in every rounding, so this is the
+            // maximum of the scaled scores of the half row
+            const float mt = (mx == -INFINITY) ? -INFINITY : __fmul_rn(mx, f);
+            xm[(sb * 2 + half) * 128 + row] = mt;
+            named_bar_sync(1 + quarter, 64);                // the two halves of these 32 rows
+            const float m_new = fmaxf(m_run, fmaxf(xm[(sb * 2 + 0) * 128 + row], xm[(sb * 2 + 1) * 128 + row]));
             const float alpha = ex2_approx(m_run - m_new);  // first tile: 2^-inf = 0
             const float nb = kLog2SP - m_new;               // P is produced pre-scaled by 448
 
-            uint32_t pk[32];
-            float ts0 = 0.f, ts1 = 0.f, ts2 = 0.f, ts3 = 0.f;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const float f = (c < 2) ? f0 : f1;
-#pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    const int col = c * 32 + i;
-                    float e0 = ex2_approx(fmaf(__uint_as_float(s[c][i + 0]), f, nb));
-                    float e1 = ex2_approx(fmaf(__uint_as_float(s[c][i + 1]), f, nb));
-                    float e2 = ex2_approx(fmaf(__uint_as_float(s[c][i + 2]), f, nb));
-                    float e3 = ex2_approx(fmaf(__uint_as_float(s[c][i + 3]), f, nb));
-                    if (valid < 128) {
-                        e0 = (col + 0 < valid) ? e0 : 0.f;
-                        e1 = (col + 1 < valid) ? e1 : 0.f;
-                        e2 = (col + 2 < valid) ? e2 : 0.f;
-                        e3 = (col + 3 < valid) ? e3 : 0.f;
-                    }
-                    ts0 += e0; ts1 += e1; ts2 += e2; ts3 += e3;
-                    pk[col >> 2] = pack_e4m3x4(e0, e1, e2, e3);
+            uint32_t pk[16];
+            float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
+            auto quad = [&](const uint32_t (&src)[32], int i, int col, bool masked) {
+                float e0, e1, e2, e3;
+                fma2_bc(e0, e1, __uint_as_float(src[i]), __uint_as_float(src[i + 1]), f, nb);
+                fma2_bc(e2, e3, __uint_as_float(src[i + 2]), __uint_as_float(src[i + 3]), f, nb);
+                if (masked) {
+                    e0 = (col + 0 < lim) ? e0 : -INFINITY;
+                    e1 = (col + 1 < lim) ? e1 : -INFINITY;
+                    e2 = (col + 2 < lim) ? e2 : -INFINITY;
+                    e3 = (col + 3 < lim) ? e3 : -INFINITY;
                 }
+                e0 = ex2_approx(e0); e1 = ex2_approx(e1); e2 = ex2_approx(e2); e3 = ex2_approx(e3);
+                add2(sa0, sa1, e0, e1);
+                add2(sb0, sb1, e2, e3);
+                pk[col >> 2] = pack_e4m3x4(e0, e1, e2, e3);
+            };
+            if (lim >= 64) {
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) { quad(s0, i, i, false); quad(s1, i, i + 32, false); }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) { quad(s0, i, i, true); quad(s1, i, i + 32, true); }
             }
-            const float tile_sum = (ts0 + ts1) + (ts2 + ts3);
+            const float tile_sum = (sa0 + sa1) + (sb0 + sb1);
 
             if (t >= 2 && !warp_wait(bar(B_PFREE + sb), ((t >> 1) - 1) & 1, abort_flag)) {
                 if (lane == 0) record_failure(p, abort_flag, R_SOFTMAX, t);
                 ok = false;
                 break;
             }
-            tmem_st32(tmem + lane_base + TM_P + sb * 32, pk);
+            tmem_st16(tmem + lane_base + TM_P + sb * 32 + half * 16, pk);
             tmem_wait_st();
-            if (t >= 2 && !warp_wait(bar(B_AFREE + sb), ((t >> 1) - 1) & 1, abort_flag)) {
-                if (lane == 0) record_failure(p, abort_flag, R_SOFTMAX, t);
-                ok = false;
-                break;
+            if (half == 0) {
+                if (t >= 2 && !warp_wait(bar(B_AFREE + sb), ((t >> 1) - 1) & 1, abort_flag)) {
+                    if (lane == 0) record_failure(p, abort_flag, R_SOFTMAX, t);
+                    ok = false;
+                    break;
+                }
+                alpha_s[sb * 128 + row] = alpha;
             }
-            alpha_s[sb * 128 + row] = alpha;
             tc_fence_before();
             mbar_arrive(bar(B_PFULL + sb));
-            mbar_arrive(bar(B_AFULL + sb));
+            if (half == 0) mbar_arrive(bar(B_AFULL + sb));
             l_run = fmaf(l_run, alpha, tile_sum);
             m_run = m_new;
         }
         if (!kCapture && ok) {
-            l_s[row] = l_run;
+            l_s[half * 128 + row] = l_run;
             mbar_arrive(bar(B_LFULL));
         }
-    } else if (warp < 8) {
+    } else if (warp < 16) {
         // ===================================================== correction + epilogue
         if (!kCapture) {
-            const int row = threadIdx.x - 128;
-            const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
-            vs_s[row] = p.v_scale[(int64_t)bh * kD + row];
-            named_bar_sync(1, 128);
-            float ro[128];
+            const int quarter = (warp - 8) & 3, half = (warp - 8) >> 2;
+            const int row = quarter * 32 + lane;
+            const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+            if (half == 0) vs_s[row] = p.v_scale[(int64_t)bh * kD + row];
+            named_bar_sync(5, 256);
+            float ro[64];
 #pragma unroll
-            for (int i = 0; i < 128; ++i) ro[i] = 0.f;
+            for (int i = 0; i < 64; ++i) ro[i] = 0.f;
             bool ok = true;
             for (int t = 0; t < T; ++t) {
                 const int sb = t & 1;
@@ -329,6 +334,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 }
                 const float alpha = alpha_s[sb * 128 + row];
                 mbar_arrive(bar(B_AFREE + sb));
+                const bool unit = __all_sync(0xffffffffu, alpha == 1.0f);   // RN(RO * 1) == RO
                 if (!warp_wait(bar(B_PVFULL), t & 1, abort_flag)) {
                     if (lane == 0) record_failure(p, abort_flag, R_CORRECT, t);
                     ok = false;
@@ -337,29 +343,37 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 tc_fence_after();
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(tmem + lane_base + TM_PV + c * 32, v);
+                    uint32_t v[16];
+                    tmem_ld16(tmem + lane_base + TM_PV + half * 64 + c * 16, v);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        ro[c * 32 + i] = fmaf(ro[c * 32 + i], alpha, fp16_round(__uint_as_float(v[i])));
+                    for (int i = 0; i < 16; i += 2) {
+                        // PV tile sum rounded to FP16, then RO = RN(RN(RO * alpha) + PV16)
+                        const __half2 h2 = __floats2half2_rn(__uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+                        float& r0 = ro[c * 16 + i];
+                        float& r1 = ro[c * 16 + i + 1];
+                        if (!unit) mul2_s(r0, r1, alpha);
+                        add_f16x2_to(r0, r1, *reinterpret_cast<const uint32_t*>(&h2));
+                    }
                 }
                 tc_fence_before();
                 mbar_arrive(bar(B_PVFREE));
             }
             if (ok && warp_wait(bar(B_LFULL), 0, abort_flag)) {
-                const float rl = __frcp_rn(l_s[row]);     // l carries the 448 scale of P
+                // l carries the 448 scale of P, so (RO / l) * v_scale is the output
+                const float rl = __frcp_rn(l_s[row] + l_s[128 + row]);
                 const int r = q0 + row;
                 if (r < lq) {
-                    uint4* dst = reinterpret_cast<uint4*>(p.o + b * p.osb + h * p.osh + (int64_t)r * p.osn);
+                    uint4* dst = reinterpret_cast<uint4*>(p.o + b * p.osb + h * p.osh + (int64_t)r * p.osn +
+                                                          half * 64);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
+                    for (int i = 0; i < 8; ++i) {
                         uint32_t w[4];
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             const int d = i * 8 + j * 2;
-                            const float o0 = __fmul_rn(__fmul_rn(ro[d], rl), vs_s[d]);
-                            const float o1 = __fmul_rn(__fmul_rn(ro[d + 1], rl), vs_s[d + 1]);
+                            const float o0 = __fmul_rn(__fmul_rn(ro[d], rl), vs_s[half * 64 + d]);
+                            const float o1 = __fmul_rn(__fmul_rn(ro[d + 1], rl), vs_s[half * 64 + d + 1]);
                             const __nv_bfloat162 pr = __floats2bfloat162_rn(o0, o1);
                             w[j] = *reinterpret_cast<const uint32_t*>(&pr);
                         }
@@ -370,7 +384,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (lane == 0) record_failure(p, abort_flag, R_CORRECT, T);
             }
         }
-    } else if (warp == 8) {
+    } else if (warp == kWarpProducer) {
         // ===================================================== TMA producer
         if (lane == 0) {
             const uint32_t sQ = sbase + OFF_Q;
@@ -420,7 +434,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     if (last_v[i] >= 0) mbar_wait(bar(B_VFULL + i), (last_v[i] / kNV) & 1, no_abort);
         }
     } else {
-        // ===================================================== MMA issuer (warp 9)
+        // ===================================================== MMA issuer
         if (lane == 0) {
             constexpr uint32_t kIdescQK = idesc_f32acc(0u, 128u, 128u);   // F16 x F16 -> F32
             constexpr uint32_t kIdescPV = idesc_f32acc(0u, 128u, 128u);   // E4M3 x E4M3 -> F32
@@ -477,7 +491,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == kWarpMma) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
