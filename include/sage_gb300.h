@@ -43,7 +43,9 @@ enum sage_status {
     SAGE_ERR_UNSUPPORTED = -2,  /* D != 128, misaligned pointer or stride */
     SAGE_ERR_LAUNCH = -3,       /* CUDA reported an error at launch */
     SAGE_ERR_TIMEOUT = -4,      /* device: a bounded wait inside a kernel ran out */
-    SAGE_ERR_DRIVER = -5        /* driver entry point for TMA descriptors missing */
+    SAGE_ERR_DRIVER = -5,       /* driver entry point for TMA descriptors missing */
+    SAGE_ERR_SCRATCH = -6       /* problem needs more scratch than the fixed buffer
+                                   of sage_prep_qkv_noalloc holds */
 };
 
 /* Logical [B, H, N, D] BF16 tensor given by its element strides; the D stride
@@ -157,6 +159,33 @@ const char* sage_status_string(int code);
 /* Number of kernel launches the last successful sage_prep_qkv / sage_attn_fwd
  * call enqueued (for launch accounting). */
 int sage_last_launch_count(void);
+
+/* Preparation for callers that cannot allocate device memory.  The paper has
+ * no counterpart: this is a deployment variant of sage_prep_qkv.  Some
+ * callers cannot call cudaMalloc for the scratch sage_prep_qkv needs, for
+ * example a plugin of an inference engine whose enqueue hook receives only
+ * its input and output pointers, or host code that runs while the device
+ * memory pool is fully committed.  This entry point takes the same arguments
+ * and fills the same outputs bit for bit, but ignores out->workspace and uses
+ * a fixed 16 MiB device array inside the library instead, which every GPU that
+ * loads the library holds until the process exits.
+ *  - Allocates nothing (no cudaMalloc/cudaFree, no allocating library call).
+ *  - The first call on a device looks up that device's address of the array
+ *    (cudaGetSymbolAddress); make that first call before any stream capture.
+ *  - All calls on a device share the array, which keeps the last call's
+ *    contents; the kernels write every scratch word before reading it, so no
+ *    clearing is needed.  Calls whose kernels may overlap on the GPU (e.g. on
+ *    unordered streams) race on the array: order them.
+ *  - Returns SAGE_ERR_SCRATCH, enqueueing nothing, when the problem needs more
+ *    than sage_prep_noalloc_capacity() bytes of scratch (the workspace size
+ *    sage_buffer_sizes reports). */
+int sage_prep_qkv_noalloc(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
+                          int B, int H, int Nq, int Nkv, int D,
+                          const int32_t* q_len, const int32_t* kv_len,
+                          const sage_prep_buffers* out, void* stream);
+
+/* Bytes of scratch available to sage_prep_qkv_noalloc (16 MiB). */
+size_t sage_prep_noalloc_capacity(void);
 
 /* Test hook for the failure-detection tests: mode 1 makes the next
  * sage_attn_fwd launch withhold its V tile copies, so the MMA issuer's

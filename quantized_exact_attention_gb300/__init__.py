@@ -23,13 +23,15 @@ SAGE_ERR_UNSUPPORTED = -2
 SAGE_ERR_LAUNCH = -3
 SAGE_ERR_TIMEOUT = -4
 SAGE_ERR_DRIVER = -5
+SAGE_ERR_SCRATCH = -6
 
 D_HEAD = 128
 
 # Names the header declares (checked by the CPU tests against the .so exports).
 EXPORTED = ("sage_buffer_sizes", "sage_prep_qkv", "sage_attn_fwd", "sage_qk_int32",
             "sage_attention_host", "sage_get_device_status", "sage_status_string",
-            "sage_last_launch_count", "sage_debug_inject_fault")
+            "sage_last_launch_count", "sage_debug_inject_fault", "sage_prep_qkv_noalloc",
+            "sage_prep_noalloc_capacity")
 
 
 class SageError(RuntimeError):
@@ -87,9 +89,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sage_status_string.restype = ctypes.c_char_p
     lib.sage_last_launch_count.argtypes = []
     lib.sage_debug_inject_fault.argtypes = [i]
+    lib.sage_prep_qkv_noalloc.argtypes = lib.sage_prep_qkv.argtypes
+    lib.sage_prep_noalloc_capacity.argtypes = []
     for name in EXPORTED:
-        if name != "sage_status_string":
+        if name not in ("sage_status_string", "sage_prep_noalloc_capacity"):
             getattr(lib, name).restype = ctypes.c_int
+    lib.sage_prep_noalloc_capacity.restype = ctypes.c_size_t
     _lib = lib
     return lib
 
@@ -175,6 +180,22 @@ def sage_prep_qkv(q, k, v, bufs: PrepBuffers, q_len=None, kv_len=None, stream=No
     rc = load_library().sage_prep_qkv(ctypes.byref(qs), ctypes.byref(ks), ctypes.byref(vs), B, H, Nq, Nkv, D,
                                       _lens(q_len), _lens(kv_len), ctypes.byref(pb), _stream_ptr(stream))
     _check(rc, "sage_prep_qkv")
+
+
+def sage_prep_qkv_noalloc(q, k, v, bufs: PrepBuffers, q_len=None, kv_len=None, stream=None):
+    """Like sage_prep_qkv, for callers that cannot allocate device memory:
+    the library's fixed scratch array is used instead of bufs.workspace."""
+    B, H, Nq, D = q.shape
+    Nkv = k.shape[2]
+    qs, ks, vs, pb = tensor_desc(q), tensor_desc(k), tensor_desc(v), bufs.c_struct()
+    rc = load_library().sage_prep_qkv_noalloc(ctypes.byref(qs), ctypes.byref(ks), ctypes.byref(vs), B, H, Nq,
+                                              Nkv, D, _lens(q_len), _lens(kv_len), ctypes.byref(pb),
+                                              _stream_ptr(stream))
+    _check(rc, "sage_prep_qkv_noalloc")
+
+
+def sage_prep_noalloc_capacity() -> int:
+    return int(load_library().sage_prep_noalloc_capacity())
 
 
 def sage_attn_fwd(bufs: PrepBuffers, o, q_len=None, kv_len=None, sm_scale: float = 0.0, stream=None,

@@ -275,6 +275,7 @@ const char* sage_status_string(int code) {
         case SAGE_ERR_LAUNCH: return "CUDA launch error";
         case SAGE_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
         case SAGE_ERR_DRIVER: return "driver entry point cuTensorMapEncodeTiled unavailable";
+        case SAGE_ERR_SCRATCH: return "problem needs more scratch than the no-allocation entry point holds";
         default: return "unknown status";
     }
 }
