@@ -22,11 +22,14 @@
 //               token-fastest) tiles through 3-deep rings
 //   warp 17     tensor-memory allocator and single-thread tcgen05 issuer:
 //               S_t = Q K_t^T (kind::f16, exact for INT8 codes: |sum| < 2^21
-//               < 2^24) and PV_t = P_t V_t (kind::f8f6f4, P read from tensor
-//               memory)
+//               < 2^24) and PV_t = P_t V_t (kind::f8f6f4 with an FP16
+//               accumulator -- the "FP16 PV" level of the two-level
+//               accumulation -- P read from tensor memory)
 //
-// Tensor memory (512 columns x 128 lanes): S double buffer [0,256), PV
-// [256,384), P double buffer [384,448) (4 e4m3 values per 32-bit column).
+// Tensor memory (512 columns x 128 lanes): S double buffer [0,256), the e4m3
+// P of a tile overwriting the first 32 columns of its S buffer (4 values per
+// 32-bit column), and a PV double buffer [256,512) of FP16 tile sums (one per
+// column) so the correction of tile t overlaps the PV MMA of tile t+1.
 //
 // Every mbarrier wait is bounded (sage_ptx.cuh); a wait that runs out records
 // SAGE_ERR_TIMEOUT in the device status words, raises a CTA-wide abort flag,
@@ -67,10 +70,9 @@ enum Bar : uint32_t {
     B_SFULL = B_VEMPTY + kNV,
     B_SFREE = B_SFULL + 2,
     B_PFULL = B_SFREE + 2,
-    B_PFREE = B_PFULL + 2,
-    B_PVFULL = B_PFREE + 2,
-    B_PVFREE = B_PVFULL + 1,
-    B_AFULL = B_PVFREE + 1,
+    B_PVFULL = B_PFULL + 2,
+    B_PVFREE = B_PVFULL + 2,
+    B_AFULL = B_PVFREE + 2,
     B_AFREE = B_AFULL + 2,
     B_LFULL = B_AFREE + 2,
     B_DRAIN = B_LFULL + 1,
@@ -87,8 +89,11 @@ constexpr uint32_t kSmemUsed = OFF_ABORT + 16;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;                          // + alignment slack
 
 constexpr uint32_t TM_S = 0;        // S buffer b at column 128*b
-constexpr uint32_t TM_PV = 256;
-constexpr uint32_t TM_P = 384;      // P buffer b at column 384 + 32*b
+constexpr uint32_t TM_PV = 256;     // PV buffer b at column 256 + 128*b (FP16, one per column)
+// P of tile t is written over the first 32 columns of S buffer t%2 once both
+// halves of every row have read their S values; the next QK into that buffer
+// is issued after the PV MMA that reads P, and tcgen05.mma executes in issue
+// order.
 constexpr uint32_t kTmemCols = 512;
 
 constexpr float kLog2SP = 8.807354922057604f;   // log2(448)
@@ -168,12 +173,11 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             mbar_init(bar(B_SFULL + i), 1);
             mbar_init(bar(B_SFREE + i), 256);     // every softmax thread
             mbar_init(bar(B_PFULL + i), 256);     // every softmax thread
-            mbar_init(bar(B_PFREE + i), 1);
             mbar_init(bar(B_AFULL + i), 128);     // softmax half 0 (writes alpha)
             mbar_init(bar(B_AFREE + i), 256);     // every correction thread
+            mbar_init(bar(B_PVFULL + i), 1);
+            mbar_init(bar(B_PVFREE + i), 256);    // every correction thread
         }
-        mbar_init(bar(B_PVFULL), 1);
-        mbar_init(bar(B_PVFREE), 256);            // every correction thread
         mbar_init(bar(B_LFULL), 256);             // every softmax thread
         mbar_init(bar(B_DRAIN), 1);
         fence_mbar_init();
@@ -201,10 +205,14 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const float qs = p.q_scale[(int64_t)bh * p.nq_blocks + qtile];
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
+        // this half's 64-key scale block of tile t is 2t + half; load one tile ahead
+        const float* kscale = p.k_scale + (int64_t)bh * p.nk_blocks;
+        float ks_next = (half * 64 < lk) ? kscale[half] : 0.f;
         for (int t = 0; t < T; ++t) {
             const int sb = t & 1;
-            const int kb = 2 * t + half;                    // this half's 64-key scale block
-            const float ks = (kb * 64 < lk) ? p.k_scale[(int64_t)bh * p.nk_blocks + kb] : 0.f;
+            const float ks = ks_next;
+            const int kb_next = 2 * (t + 1) + half;
+            ks_next = (kb_next * 64 < lk) ? kscale[kb_next] : 0.f;
             const float f = __fmul_rn(__fmul_rn(qs, ks), p.c);
             if (!warp_wait(bar(B_SFULL + sb), (t >> 1) & 1, abort_flag)) {
                 if (lane == 0) record_failure(p, abort_flag, R_SOFTMAX, t);
@@ -257,7 +265,11 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // maximum of the scaled scores of the half row
             const float mt = (mx == -INFINITY) ? -INFINITY : __fmul_rn(mx, f);
             xm[(sb * 2 + half) * 128 + row] = mt;
-            named_bar_sync(1 + quarter, 64);                // the two halves of these 32 rows
+            // The two halves of these 32 rows meet here.  Both have read their S
+            // values (tcgen05.wait::ld + fence before the s_free arrival), so
+            // after this barrier either half may overwrite S columns with P.
+            named_bar_sync(1 + quarter, 64);
+            tc_fence_after();
             const float m_new = fmaxf(m_run, fmaxf(xm[(sb * 2 + 0) * 128 + row], xm[(sb * 2 + 1) * 128 + row]));
             const float alpha = ex2_approx(m_run - m_new);  // first tile: 2^-inf = 0
             const float nb = kLog2SP - m_new;               // P is produced pre-scaled by 448
@@ -288,12 +300,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
             const float tile_sum = (sa0 + sa1) + (sb0 + sb1);
 
-            if (t >= 2 && !warp_wait(bar(B_PFREE + sb), ((t >> 1) - 1) & 1, abort_flag)) {
-                if (lane == 0) record_failure(p, abort_flag, R_SOFTMAX, t);
-                ok = false;
-                break;
-            }
-            tmem_st16(tmem + lane_base + TM_P + sb * 32 + half * 16, pk);
+            tmem_st16(tmem + lane_base + TM_S + sb * 128 + half * 16, pk);
             tmem_wait_st();
             if (half == 0) {
                 if (t >= 2 && !warp_wait(bar(B_AFREE + sb), ((t >> 1) - 1) & 1, abort_flag)) {
@@ -335,29 +342,30 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 const float alpha = alpha_s[sb * 128 + row];
                 mbar_arrive(bar(B_AFREE + sb));
                 const bool unit = __all_sync(0xffffffffu, alpha == 1.0f);   // RN(RO * 1) == RO
-                if (!warp_wait(bar(B_PVFULL), t & 1, abort_flag)) {
+                if (!warp_wait(bar(B_PVFULL + sb), (t >> 1) & 1, abort_flag)) {
                     if (lane == 0) record_failure(p, abort_flag, R_CORRECT, t);
                     ok = false;
                     break;
                 }
                 tc_fence_after();
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t v[16];
-                    tmem_ld16(tmem + lane_base + TM_PV + half * 64 + c * 16, v);
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t v[16];                         // FP16 tile sums, two per register
+                    tmem_ld32_pack16(tmem + lane_base + TM_PV + sb * 128 + half * 64 + c * 32, v);
                     tmem_wait_ld();
+                    if (c == 1) {
+                        tc_fence_before();
+                        mbar_arrive(bar(B_PVFREE + sb));
+                    }
 #pragma unroll
-                    for (int i = 0; i < 16; i += 2) {
-                        // PV tile sum rounded to FP16, then RO = RN(RN(RO * alpha) + PV16)
-                        const __half2 h2 = __floats2half2_rn(__uint_as_float(v[i]), __uint_as_float(v[i + 1]));
-                        float& r0 = ro[c * 16 + i];
-                        float& r1 = ro[c * 16 + i + 1];
+                    for (int i = 0; i < 16; ++i) {
+                        // RO = RN(RN(RO * alpha) + PV16)
+                        float& r0 = ro[c * 32 + 2 * i];
+                        float& r1 = ro[c * 32 + 2 * i + 1];
                         if (!unit) mul2_s(r0, r1, alpha);
-                        add_f16x2_to(r0, r1, *reinterpret_cast<const uint32_t*>(&h2));
+                        add_f16x2_to(r0, r1, v[i]);
                     }
                 }
-                tc_fence_before();
-                mbar_arrive(bar(B_PVFREE));
             }
             if (ok && warp_wait(bar(B_LFULL), 0, abort_flag)) {
                 // l carries the 448 scale of P, so (RO / l) * v_scale is the output
@@ -437,7 +445,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // ===================================================== MMA issuer
         if (lane == 0) {
             constexpr uint32_t kIdescQK = idesc_f32acc(0u, 128u, 128u);   // F16 x F16 -> F32
-            constexpr uint32_t kIdescPV = idesc_f32acc(0u, 128u, 128u);   // E4M3 x E4M3 -> F32
+            constexpr uint32_t kIdescPV = idesc_f16acc(0u, 128u, 128u);   // E4M3 x E4M3 -> F16
             const uint32_t sQ = sbase + OFF_Q;
             bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag);
             int fail_tile = 0;
@@ -463,15 +471,14 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 const int st = t % kNV;
                 if (!mbar_wait(bar(B_PFULL + sb), (t >> 1) & 1, abort_flag)) return false;
                 if (!mbar_wait(bar(B_VFULL + st), (t / kNV) & 1, abort_flag)) return false;
-                if (t >= 1 && !mbar_wait(bar(B_PVFREE), (t - 1) & 1, abort_flag)) return false;
+                if (t >= 2 && !mbar_wait(bar(B_PVFREE + sb), ((t >> 1) - 1) & 1, abort_flag)) return false;
                 tc_fence_after();
                 const uint32_t sV = sbase + OFF_V + st * kTileVBytes;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_f8_ts(tmem + TM_PV, tmem + TM_P + sb * 32 + kk * 8, sdesc_sw128(sV + kk * 32),
+                    mma_f8_ts(tmem + TM_PV + sb * 128, tmem + TM_S + sb * 128 + kk * 8, sdesc_sw128(sV + kk * 32),
                               kIdescPV, kk > 0 ? 1u : 0u);
-                mma_commit(bar(B_PVFULL));
-                mma_commit(bar(B_PFREE + sb));
+                mma_commit(bar(B_PVFULL + sb));
                 mma_commit(bar(B_VEMPTY + st));
                 return true;
             };
