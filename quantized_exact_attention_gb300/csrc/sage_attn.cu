@@ -449,37 +449,45 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const uint32_t sQ = sbase + OFF_Q;
             bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag);
             int fail_tile = 0;
+            // Shared-memory descriptors are built once.  Their start-address field
+            // holds (address >> 4) in the low 14 bits; every operand lies below
+            // 256 KB, so adding (byte offset >> 4) never carries out of the field.
+            const uint64_t dQ = sdesc_sw128(sQ);
+            const uint64_t dK = sdesc_sw128(sbase + OFF_K);
+            const uint64_t dV = sdesc_sw128(sbase + OFF_V);
+            int k_st = 0, k_ph = 0, v_st = 0, v_ph = 0;   // ring stage and phase of the next K / V tile
             auto issue_qk = [&](int t) -> bool {
-                const int st = t % kNK;
                 const int sb = t & 1;
-                if (!mbar_wait(bar(B_KFULL + st), (t / kNK) & 1, abort_flag)) return false;
+                if (!mbar_wait(bar(B_KFULL + k_st), k_ph, abort_flag)) return false;
                 if (t >= 2 && !mbar_wait(bar(B_SFREE + sb), ((t >> 1) - 1) & 1, abort_flag)) return false;
                 tc_fence_after();
-                const uint32_t sK = sbase + OFF_K + st * kTileKBytes;
+                const uint64_t bK = dK + (uint64_t)(k_st * (kTileKBytes >> 4));
+                const uint32_t dS = tmem + TM_S + sb * 128;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                    mma_f16_ss(tmem + TM_S + sb * 128, sdesc_sw128(sQ + off), sdesc_sw128(sK + off),
-                               kIdescQK, kk > 0 ? 1u : 0u);
+                    const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+                    mma_f16_ss(dS, dQ + off, bK + off, kIdescQK, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(B_SFULL + sb));
-                mma_commit(bar(B_KEMPTY + st));
+                mma_commit(bar(B_KEMPTY + k_st));
+                if (++k_st == kNK) { k_st = 0; k_ph ^= 1; }
                 return true;
             };
             auto issue_pv = [&](int t) -> bool {
                 const int sb = t & 1;
-                const int st = t % kNV;
                 if (!mbar_wait(bar(B_PFULL + sb), (t >> 1) & 1, abort_flag)) return false;
-                if (!mbar_wait(bar(B_VFULL + st), (t / kNV) & 1, abort_flag)) return false;
+                if (!mbar_wait(bar(B_VFULL + v_st), v_ph, abort_flag)) return false;
                 if (t >= 2 && !mbar_wait(bar(B_PVFREE + sb), ((t >> 1) - 1) & 1, abort_flag)) return false;
                 tc_fence_after();
-                const uint32_t sV = sbase + OFF_V + st * kTileVBytes;
+                const uint64_t bV = dV + (uint64_t)(v_st * (kTileVBytes >> 4));
+                const uint32_t dPV = tmem + TM_PV + sb * 128;
+                const uint32_t aP = tmem + TM_S + sb * 128;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_f8_ts(tmem + TM_PV + sb * 128, tmem + TM_S + sb * 128 + kk * 8, sdesc_sw128(sV + kk * 32),
-                              kIdescPV, kk > 0 ? 1u : 0u);
+                    mma_f8_ts(dPV, aP + kk * 8, bV + (uint64_t)(kk * (32 >> 4)), kIdescPV, kk > 0 ? 1u : 0u);
                 mma_commit(bar(B_PVFULL + sb));
-                mma_commit(bar(B_VEMPTY + st));
+                mma_commit(bar(B_VEMPTY + v_st));
+                if (++v_st == kNV) { v_st = 0; v_ph ^= 1; }
                 return true;
             };
             if (ok) ok = issue_qk(0);
