@@ -26,10 +26,11 @@
 //               accumulator -- the "FP16 PV" level of the two-level
 //               accumulation -- P read from tensor memory)
 //
-// Tensor memory (512 columns x 128 lanes): S double buffer [0,256), the e4m3
+// Tensor memory (512 columns x 128 lanes): three S buffers [0,384), the e4m3
 // P of a tile overwriting the first 32 columns of its S buffer (4 values per
-// 32-bit column), and a PV double buffer [256,512) of FP16 tile sums (one per
-// column) so the correction of tile t overlaps the PV MMA of tile t+1.
+// 32-bit column), and one PV buffer [384,512) of FP16 tile sums (one per
+// column).  Three S/P buffers let QK run two tiles ahead of PV, so the
+// softmax of tile t+1 never waits for the PV MMA of tile t-1.
 //
 // Every mbarrier wait is bounded (sage_ptx.cuh); a wait that runs out records
 // SAGE_ERR_TIMEOUT in the device status words, raises a CTA-wide abort flag,
@@ -50,6 +51,7 @@ constexpr int kWarpProducer = 16;
 constexpr int kWarpMma = 17;
 constexpr int kNK = 3;              // K ring depth
 constexpr int kNV = 3;              // V ring depth
+constexpr int kNS = 3;              // S/P buffers in tensor memory
 constexpr uint32_t kTileQBytes = 128 * 128 * 2;
 constexpr uint32_t kTileKBytes = 128 * 128 * 2;
 constexpr uint32_t kTileVBytes = 128 * 128;
@@ -67,14 +69,15 @@ enum Bar : uint32_t {
     B_KEMPTY = B_KFULL + kNK,
     B_VFULL = B_KEMPTY + kNK,
     B_VEMPTY = B_VFULL + kNV,
-    B_SFULL = B_VEMPTY + kNV,
-    B_SFREE = B_SFULL + 2,
-    B_PFULL = B_SFREE + 2,
-    B_PVFULL = B_PFULL + 2,
-    B_PVFREE = B_PVFULL + 2,
-    B_AFULL = B_PVFREE + 2,
+    B_SFULL = B_VEMPTY + kNV,   // [3] S/P buffers
+    B_SFREE = B_SFULL + kNS,
+    B_PFULL = B_SFREE + kNS,
+    B_PVFULL = B_PFULL + kNS,   // single PV buffer
+    B_PVFREE = B_PVFULL + 1,
+    B_AFULL = B_PVFREE + 1,
     B_AFREE = B_AFULL + 2,
-    B_LFULL = B_AFREE + 2,
+    B_XM = B_AFREE + 2,         // [buf][quarter]: the two halves of 32 rows exchanged maxima
+    B_LFULL = B_XM + 8,
     B_DRAIN = B_LFULL + 1,
     B_COUNT = B_DRAIN + 1
 };
@@ -88,8 +91,8 @@ constexpr uint32_t OFF_ABORT = OFF_TMEM + 16;                              // in
 constexpr uint32_t kSmemUsed = OFF_ABORT + 16;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;                          // + alignment slack
 
-constexpr uint32_t TM_S = 0;        // S buffer b at column 128*b
-constexpr uint32_t TM_PV = 256;     // PV buffer b at column 256 + 128*b (FP16, one per column)
+constexpr uint32_t TM_S = 0;        // S buffer b (0..2) at column 128*b
+constexpr uint32_t TM_PV = 384;     // PV buffer (FP16 tile sums, one per column)
 // P of tile t is written over the first 32 columns of S buffer t%2 once both
 // halves of every row have read their S values; the next QK into that buffer
 // is issued after the PV MMA that reads P, and tcgen05.mma executes in issue
@@ -169,14 +172,17 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         mbar_init(bar(B_QFULL), 1);
         for (int i = 0; i < kNK; ++i) { mbar_init(bar(B_KFULL + i), 1); mbar_init(bar(B_KEMPTY + i), 1); }
         for (int i = 0; i < kNV; ++i) { mbar_init(bar(B_VFULL + i), 1); mbar_init(bar(B_VEMPTY + i), 1); }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kNS; ++i) {
             mbar_init(bar(B_SFULL + i), 1);
             mbar_init(bar(B_SFREE + i), 256);     // every softmax thread
             mbar_init(bar(B_PFULL + i), 256);     // every softmax thread
+        }
+        mbar_init(bar(B_PVFULL), 1);
+        mbar_init(bar(B_PVFREE), 256);            // every correction thread
+        for (int i = 0; i < 8; ++i) mbar_init(bar(B_XM + i), 64);    // both halves of 32 rows
+        for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B_AFULL + i), 128);     // softmax half 0 (writes alpha)
             mbar_init(bar(B_AFREE + i), 256);     // every correction thread
-            mbar_init(bar(B_PVFULL + i), 1);
-            mbar_init(bar(B_PVFREE + i), 256);    // every correction thread
         }
         mbar_init(bar(B_LFULL), 256);             // every softmax thread
         mbar_init(bar(B_DRAIN), 1);
@@ -208,24 +214,25 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // this half's 64-key scale block of tile t is 2t + half; load one tile ahead
         const float* kscale = p.k_scale + (int64_t)bh * p.nk_blocks;
         float ks_next = (half * 64 < lk) ? kscale[half] : 0.f;
-        for (int t = 0; t < T; ++t) {
+        int s3 = 0, s3ph = 0;                               // S/P buffer of tile t and its phase
+        for (int t = 0; t < T; ++t, s3 = (s3 == kNS - 1) ? 0 : s3 + 1, s3ph ^= (s3 == 0) ? 1 : 0) {
             const int sb = t & 1;
             const float ks = ks_next;
             const int kb_next = 2 * (t + 1) + half;
             ks_next = (kb_next * 64 < lk) ? kscale[kb_next] : 0.f;
             const float f = __fmul_rn(__fmul_rn(qs, ks), p.c);
-            if (!warp_wait(bar(B_SFULL + sb), (t >> 1) & 1, abort_flag)) {
+            if (!warp_wait(bar(B_SFULL + s3), s3ph, abort_flag)) {
                 if (lane == 0) record_failure(p, abort_flag, R_SOFTMAX, t);
                 ok = false;
                 break;
             }
             tc_fence_after();
             uint32_t s0[32], s1[32];
-            tmem_ld32(tmem + lane_base + TM_S + sb * 128 + half * 64, s0);
-            tmem_ld32(tmem + lane_base + TM_S + sb * 128 + half * 64 + 32, s1);
+            tmem_ld32(tmem + lane_base + TM_S + s3 * 128 + half * 64, s0);
+            tmem_ld32(tmem + lane_base + TM_S + s3 * 128 + half * 64 + 32, s1);
             tmem_wait_ld();
             tc_fence_before();
-            mbar_arrive(bar(B_SFREE + sb));
+            mbar_arrive(bar(B_SFREE + s3));
             const int lim = lk - t * 128 - half * 64;       // valid columns of this half (may be <= 0)
 
             if (kCapture) {
@@ -268,7 +275,12 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // The two halves of these 32 rows meet here.  Both have read their S
             // values (tcgen05.wait::ld + fence before the s_free arrival), so
             // after this barrier either half may overwrite S columns with P.
-            named_bar_sync(1 + quarter, 64);
+            mbar_arrive(bar(B_XM + sb * 4 + quarter));
+            if (!warp_wait(bar(B_XM + sb * 4 + quarter), (t >> 1) & 1, abort_flag)) {
+                if (lane == 0) record_failure(p, abort_flag, R_SOFTMAX, t);
+                ok = false;
+                break;
+            }
             tc_fence_after();
             const float m_new = fmaxf(m_run, fmaxf(xm[(sb * 2 + 0) * 128 + row], xm[(sb * 2 + 1) * 128 + row]));
             const float alpha = ex2_approx(m_run - m_new);  // first tile: 2^-inf = 0
@@ -300,7 +312,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
             const float tile_sum = (sa0 + sa1) + (sb0 + sb1);
 
-            tmem_st16(tmem + lane_base + TM_S + sb * 128 + half * 16, pk);
+            tmem_st16(tmem + lane_base + TM_S + s3 * 128 + half * 16, pk);
             tmem_wait_st();
             if (half == 0) {
                 if (t >= 2 && !warp_wait(bar(B_AFREE + sb), ((t >> 1) - 1) & 1, abort_flag)) {
@@ -311,7 +323,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 alpha_s[sb * 128 + row] = alpha;
             }
             tc_fence_before();
-            mbar_arrive(bar(B_PFULL + sb));
+            mbar_arrive(bar(B_PFULL + s3));
             if (half == 0) mbar_arrive(bar(B_AFULL + sb));
             l_run = fmaf(l_run, alpha, tile_sum);
             m_run = m_new;
@@ -342,7 +354,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 const float alpha = alpha_s[sb * 128 + row];
                 mbar_arrive(bar(B_AFREE + sb));
                 const bool unit = __all_sync(0xffffffffu, alpha == 1.0f);   // RN(RO * 1) == RO
-                if (!warp_wait(bar(B_PVFULL + sb), (t >> 1) & 1, abort_flag)) {
+                if (!warp_wait(bar(B_PVFULL), t & 1, abort_flag)) {
                     if (lane == 0) record_failure(p, abort_flag, R_CORRECT, t);
                     ok = false;
                     break;
@@ -351,11 +363,11 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     uint32_t v[16];                         // FP16 tile sums, two per register
-                    tmem_ld32_pack16(tmem + lane_base + TM_PV + sb * 128 + half * 64 + c * 32, v);
+                    tmem_ld32_pack16(tmem + lane_base + TM_PV + half * 64 + c * 32, v);
                     tmem_wait_ld();
                     if (c == 1) {
                         tc_fence_before();
-                        mbar_arrive(bar(B_PVFREE + sb));
+                        mbar_arrive(bar(B_PVFREE));
                     }
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
@@ -422,14 +434,15 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 last_v[st] = t;
                 return true;
             };
+            // Loads follow the MMA issuer's consumption order: K0, K1, then
+            // K(t+2), V(t) for every tile t.
+            ok = load_k(0);
+            if (ok && T > 1) ok = load_k(1);
+            if (!ok) record_failure(p, abort_flag, R_PRODUCER, 0);
             for (int t = 0; t < T && ok; ++t) {
-                ok = load_k(t);
-                if (ok && !kCapture && t >= 1) ok = load_v(t - 1);
+                if (t + 2 < T) ok = load_k(t + 2);
+                if (ok && !kCapture) ok = load_v(t);
                 if (!ok) record_failure(p, abort_flag, R_PRODUCER, t);
-            }
-            if (ok && !kCapture) {
-                ok = load_v(T - 1);
-                if (!ok) record_failure(p, abort_flag, R_PRODUCER, T);
             }
             // Drain: every copy issued must land before the CTA may exit.
             const int zero = 0;
@@ -456,44 +469,51 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const uint64_t dK = sdesc_sw128(sbase + OFF_K);
             const uint64_t dV = sdesc_sw128(sbase + OFF_V);
             int k_st = 0, k_ph = 0, v_st = 0, v_ph = 0;   // ring stage and phase of the next K / V tile
+            int qb = 0, qph = 0;                          // S/P buffer (and phase) of the next QK
+            int pb = 0, pph = 0;                          // S/P buffer (and phase) of the next PV
+            // QK runs two tiles ahead of PV: with three S/P buffers, QK(t+2)
+            // reuses the buffer of tile t-1, whose S the softmax has read and
+            // whose P the PV MMA issued before it (same thread, in order) reads.
             auto issue_qk = [&](int t) -> bool {
-                const int sb = t & 1;
                 if (!mbar_wait(bar(B_KFULL + k_st), k_ph, abort_flag)) return false;
-                if (t >= 2 && !mbar_wait(bar(B_SFREE + sb), ((t >> 1) - 1) & 1, abort_flag)) return false;
+                if (t >= kNS && !mbar_wait(bar(B_SFREE + qb), qph ^ 1, abort_flag)) return false;
                 tc_fence_after();
                 const uint64_t bK = dK + (uint64_t)(k_st * (kTileKBytes >> 4));
-                const uint32_t dS = tmem + TM_S + sb * 128;
+                const uint32_t dS = tmem + TM_S + qb * 128;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
                     mma_f16_ss(dS, dQ + off, bK + off, kIdescQK, kk > 0 ? 1u : 0u);
                 }
-                mma_commit(bar(B_SFULL + sb));
+                mma_commit(bar(B_SFULL + qb));
                 mma_commit(bar(B_KEMPTY + k_st));
                 if (++k_st == kNK) { k_st = 0; k_ph ^= 1; }
+                if (++qb == kNS) { qb = 0; qph ^= 1; }
                 return true;
             };
+            // The operands that are almost always ready are checked first, so
+            // that only the wait for P sits between the softmax and the PV MMA.
             auto issue_pv = [&](int t) -> bool {
-                const int sb = t & 1;
-                if (!mbar_wait(bar(B_PFULL + sb), (t >> 1) & 1, abort_flag)) return false;
                 if (!mbar_wait(bar(B_VFULL + v_st), v_ph, abort_flag)) return false;
-                if (t >= 2 && !mbar_wait(bar(B_PVFREE + sb), ((t >> 1) - 1) & 1, abort_flag)) return false;
+                if (t >= 1 && !mbar_wait(bar(B_PVFREE), (t - 1) & 1, abort_flag)) return false;
+                if (!mbar_wait(bar(B_PFULL + pb), pph, abort_flag)) return false;
                 tc_fence_after();
                 const uint64_t bV = dV + (uint64_t)(v_st * (kTileVBytes >> 4));
-                const uint32_t dPV = tmem + TM_PV + sb * 128;
-                const uint32_t aP = tmem + TM_S + sb * 128;
+                const uint32_t aP = tmem + TM_S + pb * 128;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_f8_ts(dPV, aP + kk * 8, bV + (uint64_t)(kk * (32 >> 4)), kIdescPV, kk > 0 ? 1u : 0u);
-                mma_commit(bar(B_PVFULL + sb));
+                    mma_f8_ts(tmem + TM_PV, aP + kk * 8, bV + (uint64_t)(kk * (32 >> 4)), kIdescPV, kk > 0 ? 1u : 0u);
+                mma_commit(bar(B_PVFULL));
                 mma_commit(bar(B_VEMPTY + v_st));
                 if (++v_st == kNV) { v_st = 0; v_ph ^= 1; }
+                if (++pb == kNS) { pb = 0; pph ^= 1; }
                 return true;
             };
             if (ok) ok = issue_qk(0);
+            if (ok && T > 1) ok = issue_qk(1);
             for (int t = 0; t < T && ok; ++t) {
                 fail_tile = t;
-                if (t + 1 < T) ok = issue_qk(t + 1);
+                if (t + 2 < T) ok = issue_qk(t + 2);
                 if (ok && !kCapture) ok = issue_pv(t);
             }
             if (!ok) record_failure(p, abort_flag, R_MMA, fail_tile);
