@@ -3,12 +3,16 @@
 // Verification": Q/K preparation, K smoothing, INT8 quantization, FP8 V).
 //
 // Three launches, all HBM-bound streaming kernels with 128-bit accesses:
-//   1. prep_stats     per 64-token chunk: ordered FP32 K column sums and
-//                     V column |max| (8 chunks per 128-thread block)
+//   1. prep_stats_q   per 64-token chunk: ordered FP32 K column sums and V
+//                     column |max| (16 chunks per block); and, independent
+//                     of those, the INT8 quantization of every 128-row Q block
 //   2. prep_finalize  per (b,h): chunk sums in order -> K mean; V amax ->
 //                     v_scale and its inverse
-//   3. prep_quant     Q blocks (128 rows), K blocks (64 rows) and V tiles
-//                     (64 tokens, written transposed: token index fastest)
+//   3. prep_kv        K blocks (64 rows of K - mean) and V tiles (64 tokens,
+//                     written transposed: token index fastest)
+// Loaded BF16 data stays packed in registers (8 values per 16-byte word) and
+// is widened on use, which keeps register use low enough for several blocks
+// per SM and enough bytes in flight to stream HBM.
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
@@ -16,6 +20,8 @@
 
 namespace sage {
 namespace {
+
+constexpr int kStatChunksPerBlock = 16;   // 16 chunks x 16 channel groups = 256 threads
 
 __device__ __forceinline__ int clamp_len(const int32_t* lens, int b, int n) {
     if (lens == nullptr) return n;
@@ -33,20 +39,69 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&x)[8]) {
     x[6] = bf16_lo(u.w); x[7] = bf16_hi(u.w);
 }
 
+// |x| of 8 packed BF16 values, maximum folded into m (the sign bit is cleared
+// on the packed words: BF16 -> FP32 widening is exact, so this equals the
+// maximum of |x| over the widened values)
+__device__ __forceinline__ float absmax8(const uint4& u, float m) {
+    float x[8];
+    unpack8(make_uint4(u.x & 0x7FFF7FFFu, u.y & 0x7FFF7FFFu, u.z & 0x7FFF7FFFu, u.w & 0x7FFF7FFFu), x);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) m = fmaxf(m, x[e]);
+    return m;
+}
+
 __device__ __forceinline__ uint4 ldg16(const uint16_t* p) {
     return __ldg(reinterpret_cast<const uint4*>(p));
 }
 
+__device__ __forceinline__ float block_max_256(float v, float* red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    const int w = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) red[w] = v;
+    __syncthreads();
+    float r = red[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) r = fmaxf(r, red[i]);
+    return r;
+}
+
+__device__ __forceinline__ uint32_t half_code(int c) {
+    return (uint32_t)__half_as_ushort(__int2half_rn(c));
+}
+
+__device__ __forceinline__ int int8_code(float x, float inv) {
+    int c = __float2int_rn(__fmul_rn(x, inv));
+    return c > 127 ? 127 : (c < -127 ? -127 : c);
+}
+
+// Store the INT8 codes of one row's 8 channels as FP16 images (and as INT8
+// bytes when requested).
+__device__ __forceinline__ void store_row_codes(const int (&c)[8], uint16_t* img, int8_t* bytes, int64_t off) {
+    uint4 hv;
+    hv.x = half_code(c[0]) | (half_code(c[1]) << 16);
+    hv.y = half_code(c[2]) | (half_code(c[3]) << 16);
+    hv.z = half_code(c[4]) | (half_code(c[5]) << 16);
+    hv.w = half_code(c[6]) | (half_code(c[7]) << 16);
+    *reinterpret_cast<uint4*>(img + off) = hv;
+    if (bytes != nullptr) {
+        uint2 bv;
+        bv.x = (uint32_t)(c[0] & 0xFF) | ((uint32_t)(c[1] & 0xFF) << 8) |
+               ((uint32_t)(c[2] & 0xFF) << 16) | ((uint32_t)(c[3] & 0xFF) << 24);
+        bv.y = (uint32_t)(c[4] & 0xFF) | ((uint32_t)(c[5] & 0xFF) << 8) |
+               ((uint32_t)(c[6] & 0xFF) << 16) | ((uint32_t)(c[7] & 0xFF) << 24);
+        *reinterpret_cast<uint2*>(bytes + off) = bv;
+    }
+}
+
 // ---------------------------------------------------------------------------
-// 1. Per-chunk statistics.  Thread (chunk slot cl, channel group dg) owns 8
-// channels of one 64-token chunk and walks its tokens in ascending order, so
-// every partial sum is the FP32 left-to-right sum the contract pins.
+// 1. Chunk statistics and Q quantization.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(128) prep_stats_kernel(const PrepParams p) {
-    const int b = blockIdx.z, h = blockIdx.y;
-    const int dg = threadIdx.x & 15, cl = threadIdx.x >> 4;
-    const int c = blockIdx.x * 8 + cl;
-    if (c >= p.n_chunks) return;
+// Statistics: thread (chunk slot cl, channel group dg) owns 8 channels of one
+// 64-token chunk and walks its tokens in ascending order, so every partial
+// sum is the FP32 left-to-right sum the contract pins.
+__device__ __forceinline__ void chunk_stats(const PrepParams& p, int b, int h, int c) {
+    const int dg = threadIdx.x & 15;
     const int lk = clamp_len(p.kv_len, b, p.Nkv);
     const int d0 = dg * 8;
     const int t0 = c * kMeanChunk;
@@ -57,15 +112,15 @@ __global__ void __launch_bounds__(128) prep_stats_kernel(const PrepParams p) {
     const uint16_t* kp = p.k + b * p.ksb + h * p.ksh + d0;
     const uint16_t* vp = p.v + b * p.vsb + h * p.vsh + d0;
     int t = t0;
-    for (; t + 8 <= t1; t += 8) {
-        uint4 ku[8], vu[8];
+    for (; t + 4 <= t1; t += 4) {
+        uint4 ku[4], vu[4];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < 4; ++u) {
             ku[u] = ldg16(kp + (int64_t)(t + u) * p.ksn);
             vu[u] = ldg16(vp + (int64_t)(t + u) * p.vsn);
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < 4; ++u) {
             float kx[8], vx[8];
             unpack8(ku[u], kx);
             unpack8(vu[u], vx);
@@ -95,18 +150,81 @@ __global__ void __launch_bounds__(128) prep_stats_kernel(const PrepParams p) {
     pa[1] = make_float4(a[4], a[5], a[6], a[7]);
 }
 
+// Q block: rows [r0, r0+128), one INT8 scale for the whole block.
+__device__ __forceinline__ void quant_q_block(const PrepParams& p, int b, int h, int qb, float* red) {
+    const int bh = b * p.H + h;
+    const int tid = threadIdx.x;
+    const int lq = clamp_len(p.q_len, b, p.Nq);
+    const int dg = tid & 15, rs = tid >> 4;
+    const int d0 = dg * 8, r0 = qb * kBQS;
+    uint4 xr[8];
+    float amax = 0.f;
+    const uint16_t* qp = p.q + b * p.qsb + h * p.qsh + d0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = r0 + rs + 16 * i;
+        xr[i] = (r < lq) ? ldg16(qp + (int64_t)r * p.qsn) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = absmax8(xr[i], amax);
+    amax = block_max_256(amax, red);
+    const float inv = amax > 0.f ? __fdiv_rn(127.0f, amax) : 0.f;
+    if (tid == 0) p.q_scale[(int64_t)bh * p.nq_blocks + qb] = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = r0 + rs + 16 * i;
+        if (r >= p.Nq) continue;
+        float x[8];
+        unpack8(xr[i], x);
+        int c[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) c[e] = (r < lq) ? int8_code(x[e], inv) : 0;
+        store_row_codes(c, p.q16, p.q8, ((int64_t)bh * p.Nq + r) * kD + d0);
+    }
+}
+
+__global__ void __launch_bounds__(256, 3) prep_stats_q_kernel(const PrepParams p) {
+    __shared__ float red[8];
+    const int b = blockIdx.z, h = blockIdx.y;
+    const int n_stat_blocks = (p.n_chunks + kStatChunksPerBlock - 1) / kStatChunksPerBlock;
+    if ((int)blockIdx.x < n_stat_blocks) {
+        const int c = blockIdx.x * kStatChunksPerBlock + (threadIdx.x >> 4);
+        if (c < p.n_chunks) chunk_stats(p, b, h, c);
+    } else {
+        quant_q_block(p, b, h, blockIdx.x - n_stat_blocks, red);
+    }
+}
+
 // ---------------------------------------------------------------------------
-// 2. Per-(b,h) finalisation, one thread per channel.
+// 2. Per-(b,h) finalisation, one thread per channel.  The chunk partials are
+// fetched 32 at a time (independent loads in flight) and then added strictly
+// in ascending chunk order.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(128) prep_finalize_kernel(const PrepParams p) {
     const int b = blockIdx.y, h = blockIdx.x, d = threadIdx.x;
     const int lk = clamp_len(p.kv_len, b, p.Nkv);
     const int nc = (lk + kMeanChunk - 1) / kMeanChunk;
     const int64_t base = ((int64_t)b * p.H + h) * p.n_chunks * kD + d;
+    const float* ps = p.psum + base;
+    const float* pa = p.pamax + base;
     float total = 0.f, amax = 0.f;
-    for (int c = 0; c < nc; ++c) {
-        total = __fadd_rn(total, p.psum[base + (int64_t)c * kD]);
-        amax = fmaxf(amax, p.pamax[base + (int64_t)c * kD]);
+    int c = 0;
+    for (; c + 32 <= nc; c += 32) {
+        float sv[32], av[32];
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+            sv[u] = ps[(int64_t)(c + u) * kD];
+            av[u] = pa[(int64_t)(c + u) * kD];
+        }
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+            total = __fadd_rn(total, sv[u]);
+            amax = fmaxf(amax, av[u]);
+        }
+    }
+    for (; c < nc; ++c) {
+        total = __fadd_rn(total, ps[(int64_t)c * kD]);
+        amax = fmaxf(amax, pa[(int64_t)c * kD]);
     }
     const int64_t o = ((int64_t)b * p.H + h) * kD + d;
     p.k_mean[o] = lk > 0 ? __fdiv_rn(total, (float)lk) : 0.f;
@@ -115,183 +233,115 @@ __global__ void __launch_bounds__(128) prep_finalize_kernel(const PrepParams p) 
 }
 
 // ---------------------------------------------------------------------------
-// 3. Quantization.  blockIdx.x selects the work item: Q blocks first, then
-// K blocks, then V tiles.  256 threads; thread = (row slot, 8-channel group).
+// 3. K and V quantization.  blockIdx.x selects the work item: K blocks first,
+// then V tiles.  256 threads.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float block_max_256(float v, float* red) {
+// K block: rows [r0, r0+64) of K - mean, one INT8 scale for the block.
+__device__ __forceinline__ void quant_k_block(const PrepParams& p, int b, int h, int kb, float* red) {
+    const int bh = b * p.H + h;
+    const int tid = threadIdx.x;
+    const int lk = clamp_len(p.kv_len, b, p.Nkv);
+    const int dg = tid & 15, rs = tid >> 4;
+    const int d0 = dg * 8, r0 = kb * kBKS;
+    float mean[8];
+    {
+        const float4* mp = reinterpret_cast<const float4*>(p.k_mean + (int64_t)bh * kD + d0);
+        const float4 m0 = mp[0], m1 = mp[1];
+        mean[0] = m0.x; mean[1] = m0.y; mean[2] = m0.z; mean[3] = m0.w;
+        mean[4] = m1.x; mean[5] = m1.y; mean[6] = m1.z; mean[7] = m1.w;
+    }
+    uint4 xr[4];
+    const uint16_t* kp = p.k + b * p.ksb + h * p.ksh + d0;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    const int w = threadIdx.x >> 5;
-    if ((threadIdx.x & 31) == 0) red[w] = v;
-    __syncthreads();
-    float r = red[0];
+    for (int i = 0; i < 4; ++i) {
+        const int r = r0 + rs + 16 * i;
+        xr[i] = (r < lk) ? ldg16(kp + (int64_t)r * p.ksn) : make_uint4(0, 0, 0, 0);
+    }
+    float amax = 0.f;
 #pragma unroll
-    for (int i = 1; i < 8; ++i) r = fmaxf(r, red[i]);
-    return r;
-}
-
-__device__ __forceinline__ uint32_t half_code(int c) {
-    return (uint32_t)__half_as_ushort(__int2half_rn(c));
-}
-
-__device__ __forceinline__ int int8_code(float x, float inv) {
-    int c = __float2int_rn(__fmul_rn(x, inv));
-    return c > 127 ? 127 : (c < -127 ? -127 : c);
-}
-
-// Quantize ROWS_PER_THREAD rows x 8 channels held in x[][] with the block
-// scale; store FP16 code images (and INT8 bytes when requested).
-template <int R>
-__device__ __forceinline__ void store_codes(const float (&x)[R][8], float inv, int r_first, int r_step,
-                                            int valid, int nrows, uint16_t* img, int8_t* bytes,
-                                            int64_t row_base, int d0) {
+    for (int i = 0; i < 4; ++i) {
+        const int r = r0 + rs + 16 * i;
+        if (r < lk) {
+            float x[8];
+            unpack8(xr[i], x);
 #pragma unroll
-    for (int i = 0; i < R; ++i) {
-        const int r = r_first + i * r_step;
-        if (r >= nrows) continue;
+            for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(__fsub_rn(x[e], mean[e])));
+        }
+    }
+    amax = block_max_256(amax, red);
+    const float inv = amax > 0.f ? __fdiv_rn(127.0f, amax) : 0.f;
+    if (tid == 0) p.k_scale[(int64_t)bh * p.nk_blocks + kb] = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = r0 + rs + 16 * i;
+        if (r >= p.Nkv) continue;
+        float x[8];
+        unpack8(xr[i], x);
         int c[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) c[e] = (r < valid) ? int8_code(x[i][e], inv) : 0;
-        uint4 hv;
-        hv.x = half_code(c[0]) | (half_code(c[1]) << 16);
-        hv.y = half_code(c[2]) | (half_code(c[3]) << 16);
-        hv.z = half_code(c[4]) | (half_code(c[5]) << 16);
-        hv.w = half_code(c[6]) | (half_code(c[7]) << 16);
-        const int64_t off = (row_base + r) * kD + d0;
-        *reinterpret_cast<uint4*>(img + off) = hv;
-        if (bytes != nullptr) {
-            uint2 bv;
-            bv.x = (uint32_t)(c[0] & 0xFF) | ((uint32_t)(c[1] & 0xFF) << 8) |
-                   ((uint32_t)(c[2] & 0xFF) << 16) | ((uint32_t)(c[3] & 0xFF) << 24);
-            bv.y = (uint32_t)(c[4] & 0xFF) | ((uint32_t)(c[5] & 0xFF) << 8) |
-                   ((uint32_t)(c[6] & 0xFF) << 16) | ((uint32_t)(c[7] & 0xFF) << 24);
-            *reinterpret_cast<uint2*>(bytes + off) = bv;
+        for (int e = 0; e < 8; ++e) c[e] = (r < lk) ? int8_code(__fsub_rn(x[e], mean[e]), inv) : 0;
+        store_row_codes(c, p.k16, p.k8, ((int64_t)bh * p.Nkv + r) * kD + d0);
+    }
+}
+
+// V tile: tokens [t0, t0+64) -> e4m3 per channel, stored [d][token].
+__device__ __forceinline__ void quant_v_tile(const PrepParams& p, int b, int h, int vt, uint32_t* vtile) {
+    const int bh = b * p.H + h;
+    const int tid = threadIdx.x;
+    const int lk = clamp_len(p.kv_len, b, p.Nkv);
+    const int tq = tid & 15, dg = tid >> 4;           // 4 tokens x 8 channels per thread
+    const int d0 = dg * 8, t0 = vt * 64;
+    float inv[8];
+    {
+        const float4* ip = reinterpret_cast<const float4*>(p.v_inv + (int64_t)bh * kD + d0);
+        const float4 i0 = ip[0], i1 = ip[1];
+        inv[0] = i0.x; inv[1] = i0.y; inv[2] = i0.z; inv[3] = i0.w;
+        inv[4] = i1.x; inv[5] = i1.y; inv[6] = i1.z; inv[7] = i1.w;
+    }
+    const uint16_t* vp = p.v + b * p.vsb + h * p.vsh + d0;
+    uint4 xr[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int t = t0 + tq * 4 + u;
+        xr[u] = (t < lk) ? ldg16(vp + (int64_t)t * p.vsn) : make_uint4(0, 0, 0, 0);
+    }
+    uint32_t word[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) word[e] = 0u;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int t = t0 + tq * 4 + u;
+        float x[8];
+        unpack8(xr[u], x);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const bool live = (t < lk) && (inv[e] > 0.f);
+            const __nv_fp8_storage_t c =
+                __nv_cvt_float_to_fp8(__fmul_rn(x[e], inv[e]), __NV_SATFINITE, __NV_E4M3);
+            word[e] |= (live ? (uint32_t)c : 0u) << (8 * u);
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) vtile[(d0 + e) * 20 + tq] = word[e];
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int chunk = tid + 256 * k;                // 128 rows x 4 chunks of 16 tokens
+        const int d = chunk >> 2, part = chunk & 3;
+        const int t = t0 + part * 16;
+        if (t < p.nkv_pad) {
+            const uint4 w = *reinterpret_cast<const uint4*>(&vtile[d * 20 + part * 4]);
+            *reinterpret_cast<uint4*>(p.v8t + ((int64_t)bh * kD + d) * p.nkv_pad + t) = w;
         }
     }
 }
 
-__global__ void __launch_bounds__(256) prep_quant_kernel(const PrepParams p) {
+__global__ void __launch_bounds__(256, 4) prep_kv_kernel(const PrepParams p) {
     __shared__ float red[8];
     __shared__ __align__(16) uint32_t vtile[kD * 20];   // [d][16 words of 4 tokens + 4 pad]
     const int b = blockIdx.z, h = blockIdx.y;
-    const int bh = b * p.H + h;
-    const int tid = threadIdx.x;
-    int item = blockIdx.x;
-
-    if (item < p.nq_blocks) {
-        // ---- Q block: rows [r0, r0+128), per-block INT8 scale
-        const int lq = clamp_len(p.q_len, b, p.Nq);
-        const int dg = tid & 15, rs = tid >> 4;
-        const int d0 = dg * 8, r0 = item * kBQS;
-        float x[8][8];
-        float amax = 0.f;
-        const uint16_t* qp = p.q + b * p.qsb + h * p.qsh + d0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int r = r0 + rs + 16 * i;
-            if (r < lq) {
-                unpack8(ldg16(qp + (int64_t)r * p.qsn), x[i]);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[i][e]));
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) x[i][e] = 0.f;
-            }
-        }
-        amax = block_max_256(amax, red);
-        const float inv = amax > 0.f ? __fdiv_rn(127.0f, amax) : 0.f;
-        if (tid == 0) p.q_scale[(int64_t)bh * p.nq_blocks + item] = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 0.f;
-        store_codes<8>(x, inv, r0 + rs, 16, lq, p.Nq, p.q16, p.q8, (int64_t)bh * p.Nq, d0);
-        return;
-    }
-    item -= p.nq_blocks;
-    if (item < p.nk_blocks) {
-        // ---- K block: rows [r0, r0+64) of K - mean, per-block INT8 scale
-        const int lk = clamp_len(p.kv_len, b, p.Nkv);
-        const int dg = tid & 15, rs = tid >> 4;
-        const int d0 = dg * 8, r0 = item * kBKS;
-        float mean[8];
-        {
-            const float4* mp = reinterpret_cast<const float4*>(p.k_mean + (int64_t)bh * kD + d0);
-            const float4 m0 = mp[0], m1 = mp[1];
-            mean[0] = m0.x; mean[1] = m0.y; mean[2] = m0.z; mean[3] = m0.w;
-            mean[4] = m1.x; mean[5] = m1.y; mean[6] = m1.z; mean[7] = m1.w;
-        }
-        float x[4][8];
-        float amax = 0.f;
-        const uint16_t* kp = p.k + b * p.ksb + h * p.ksh + d0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int r = r0 + rs + 16 * i;
-            if (r < lk) {
-                unpack8(ldg16(kp + (int64_t)r * p.ksn), x[i]);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    x[i][e] = __fsub_rn(x[i][e], mean[e]);
-                    amax = fmaxf(amax, fabsf(x[i][e]));
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) x[i][e] = 0.f;
-            }
-        }
-        amax = block_max_256(amax, red);
-        const float inv = amax > 0.f ? __fdiv_rn(127.0f, amax) : 0.f;
-        if (tid == 0) p.k_scale[(int64_t)bh * p.nk_blocks + item] = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 0.f;
-        store_codes<4>(x, inv, r0 + rs, 16, lk, p.Nkv, p.k16, p.k8, (int64_t)bh * p.Nkv, d0);
-        return;
-    }
-    item -= p.nk_blocks;
-    {
-        // ---- V tile: tokens [t0, t0+64) -> e4m3 per channel, stored [d][token]
-        const int lk = clamp_len(p.kv_len, b, p.Nkv);
-        const int tq = tid & 15, dg = tid >> 4;           // 4 tokens x 8 channels per thread
-        const int d0 = dg * 8, t0 = item * 64;
-        float inv[8];
-        bool nz[8];
-        {
-            const float4* ip = reinterpret_cast<const float4*>(p.v_inv + (int64_t)bh * kD + d0);
-            const float4 i0 = ip[0], i1 = ip[1];
-            inv[0] = i0.x; inv[1] = i0.y; inv[2] = i0.z; inv[3] = i0.w;
-            inv[4] = i1.x; inv[5] = i1.y; inv[6] = i1.z; inv[7] = i1.w;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) nz[e] = inv[e] > 0.f;
-        }
-        uint32_t code[8][4];                               // [channel][token]
-        const uint16_t* vp = p.v + b * p.vsb + h * p.vsh + d0;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int t = t0 + tq * 4 + u;
-            float x[8];
-            if (t < lk) {
-                unpack8(ldg16(vp + (int64_t)t * p.vsn), x);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = 0.f;
-            }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const bool live = (t < lk) && nz[e];
-                const __nv_fp8_storage_t c =
-                    __nv_cvt_float_to_fp8(__fmul_rn(x[e], inv[e]), __NV_SATFINITE, __NV_E4M3);
-                code[e][u] = live ? (uint32_t)c : 0u;
-            }
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-            vtile[(d0 + e) * 20 + tq] = code[e][0] | (code[e][1] << 8) | (code[e][2] << 16) | (code[e][3] << 24);
-        __syncthreads();
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const int chunk = tid + 256 * k;                // 128 rows x 4 chunks of 16 tokens
-            const int d = chunk >> 2, part = chunk & 3;
-            const int t = t0 + part * 16;
-            if (t < p.nkv_pad) {
-                const uint4 w = *reinterpret_cast<const uint4*>(&vtile[d * 20 + part * 4]);
-                *reinterpret_cast<uint4*>(p.v8t + ((int64_t)bh * kD + d) * p.nkv_pad + t) = w;
-            }
-        }
-    }
+    if ((int)blockIdx.x < p.nk_blocks) quant_k_block(p, b, h, blockIdx.x, red);
+    else quant_v_tile(p, b, h, blockIdx.x - p.nk_blocks, vtile);
 }
 
 }  // namespace
@@ -299,8 +349,9 @@ __global__ void __launch_bounds__(256) prep_quant_kernel(const PrepParams p) {
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t s, int* launches) {
     *launches = 0;
     {
-        dim3 grid((unsigned)((p.n_chunks + 7) / 8), (unsigned)p.H, (unsigned)p.B);
-        prep_stats_kernel<<<grid, 128, 0, s>>>(p);
+        const int n_stat_blocks = (p.n_chunks + kStatChunksPerBlock - 1) / kStatChunksPerBlock;
+        dim3 grid((unsigned)(n_stat_blocks + p.nq_blocks), (unsigned)p.H, (unsigned)p.B);
+        prep_stats_q_kernel<<<grid, 256, 0, s>>>(p);
         ++*launches;
     }
     {
@@ -310,8 +361,8 @@ cudaError_t launch_prep(const PrepParams& p, cudaStream_t s, int* launches) {
     }
     {
         const int n_vtiles = (p.nkv_pad + 63) / 64;
-        dim3 grid((unsigned)(p.nq_blocks + p.nk_blocks + n_vtiles), (unsigned)p.H, (unsigned)p.B);
-        prep_quant_kernel<<<grid, 256, 0, s>>>(p);
+        dim3 grid((unsigned)(p.nk_blocks + n_vtiles), (unsigned)p.H, (unsigned)p.B);
+        prep_kv_kernel<<<grid, 256, 0, s>>>(p);
         ++*launches;
     }
     return cudaGetLastError();
