@@ -36,6 +36,12 @@ with its justification in the design notes:
   R12 RO = RO * alpha + PV16 in FP32 every tile.
   R13 out = bf16((RO * (1/l)) * (v_scale/448)).
   R14 rows of a query with no keys are zero.
+  R15 causal masking (not on the pages; an adjacent use): key j is visible
+      to query i of a batch item iff j <= i + (Lk - Lq), i.e. the diagonal is
+      aligned to the last query and the last key (j <= i when Lq = Lk).  A
+      row that sees no key is zero, as in R14.  A tile whose keys are all
+      hidden from a row changes nothing for it (alpha = exp2(0) = 1, p = 0),
+      so the row's result is the non-causal one over its visible prefix.
 
 Precision: every step is carried out in the precision the contract names
 (FP32 via numpy float32 arithmetic, which rounds each operation to nearest
@@ -316,24 +322,40 @@ class Checkpoints:
     recip: np.ndarray | None = None
 
 
+def visible_keys(prep: Prepared, b: int, rows: np.ndarray, causal: bool) -> np.ndarray:
+    """Number of keys [0, n) each query row sees (R14; R15 when causal)."""
+    lk = int(prep.kv_len[b])
+    rows = np.asarray(rows, dtype=np.int64)
+    if not causal:
+        return np.full(len(rows), lk, dtype=np.int64)
+    lq = int(prep.q_len[b])
+    return np.clip(rows + (lk - lq) + 1, 0, lk)
+
+
 def attention_rows(prep: Prepared, b: int, h: int, rows: np.ndarray,
-                   sm_scale: float | None = None, checkpoints: Checkpoints | None = None):
+                   sm_scale: float | None = None, checkpoints: Checkpoints | None = None,
+                   causal: bool = False):
     """Output rows of one (b, h) head: float32 values of the BF16 result.
 
     rows: query indices (all < q_len[b]).  Returns (out_bf16_bits uint16
-    [len(rows), D], out float32 [len(rows), D]).
+    [len(rows), D], out float32 [len(rows), D]).  causal: R15 masking.
     """
     rows = np.asarray(rows, dtype=np.int64)
     D = prep.q8.shape[-1]
-    lk = int(prep.kv_len[b])
     nr = len(rows)
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
     c = score_factor_c(sm_scale)
+    vis = visible_keys(prep, b, rows, causal)
     if nr == 0:
         return np.zeros((0, D), np.uint16), np.zeros((0, D), F32)
-    if lk == 0:                                   # R14: no keys -> zero rows
-        return np.zeros((nr, D), np.uint16), np.zeros((nr, D), F32)
+    if np.any(vis == 0):                          # R14/R15: rows that see no key are zero
+        bits = np.zeros((nr, D), np.uint16)
+        live = vis > 0
+        if np.any(live):
+            bits[live] = attention_rows(prep, b, h, rows[live], sm_scale, checkpoints, causal)[0]
+        return bits, bf16_bits_to_f32(bits)
+    lk = int(vis.max())                           # keys [lk, kv_len) are hidden from every row
 
     q_sc = prep.q_scale[b, h][rows // BQS]                      # [nr]
     S = qk_scores(prep.q8[b, h][rows], prep.k8[b, h][:lk])      # [nr, lk] exact ints
@@ -348,6 +370,7 @@ def attention_rows(prep: Prepared, b: int, h: int, rows: np.ndarray,
         k_sc = prep.k_scale[b, h][cols // BKS]                  # [w]
         f = ((q_sc[:, None] * k_sc[None, :]).astype(F32) * c).astype(F32)
         s2 = (S[:, j0:j1].astype(F32) * f).astype(F32)          # exact int -> f32, one rounding
+        s2 = np.where(cols[None, :] < vis[:, None], s2, F32(-np.inf)).astype(F32)   # R15 mask
         m_new = np.maximum(m, np.max(s2, axis=1)).astype(F32)
         with np.errstate(invalid="ignore"):
             alpha = np.where(np.isneginf(m), F32(0.0), exp2_f32((m - m_new).astype(F32))).astype(F32)
@@ -376,7 +399,7 @@ def attention_rows(prep: Prepared, b: int, h: int, rows: np.ndarray,
     return bits, bf16_bits_to_f32(bits)
 
 
-def attention(prep: Prepared, sm_scale: float | None = None):
+def attention(prep: Prepared, sm_scale: float | None = None, causal: bool = False):
     """Full output [B, H, Nq, D] as BF16 bits (uint16); rows >= q_len are 0."""
     B, H, Nq, D = prep.q8.shape
     out = np.zeros((B, H, Nq, D), dtype=np.uint16)
@@ -384,5 +407,5 @@ def attention(prep: Prepared, sm_scale: float | None = None):
         lq = int(prep.q_len[b])
         rows = np.arange(lq)
         for h in range(H):
-            out[b, h, :lq] = attention_rows(prep, b, h, rows, sm_scale)[0]
+            out[b, h, :lq] = attention_rows(prep, b, h, rows, sm_scale, causal=causal)[0]
     return out

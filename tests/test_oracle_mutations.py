@@ -9,6 +9,7 @@ import pytest
 
 from oracle import sage_oracle as O
 from tests import test_oracle_attention as TA
+from tests import test_oracle_causal as TC
 from tests import test_oracle_formats as TF
 from tests import test_oracle_prep as TP
 
@@ -26,6 +27,21 @@ def _ties_away(x):
     d_up = np.abs(O.e4m3_decode(up) - np.abs(xv))
     tie = (d_out > 0) & (d_up == d_out) & (O.e4m3_decode(up) > below)
     return np.where(tie, (up | (out & 0x80)).astype(np.uint8), out).astype(np.uint8)
+
+
+_VISIBLE = O.visible_keys
+
+
+def _causal_top_left(prep, b, rows, causal):
+    # diagonal through (0, 0) instead of through the last query and last key
+    if not causal:
+        return _VISIBLE(prep, b, rows, causal)
+    return np.clip(np.asarray(rows, np.int64) + 1, 0, int(prep.kv_len[b]))
+
+
+def _causal_strict(prep, b, rows, causal):
+    # j < i + (Lk - Lq): the diagonal key itself hidden
+    return np.maximum(_VISIBLE(prep, b, rows, causal) - (1 if causal else 0), 0)
 
 
 def _mean_over_channels(k, kv_len):
@@ -56,6 +72,12 @@ MUTATIONS = {
     "q_scale_block_64": (
         lambda mp: mp.setattr(O, "BQS", 64),
         TP.test_prepare_shapes_and_varlen_padding),
+    "causal_diagonal_top_left": (
+        lambda mp: mp.setattr(O, "visible_keys", _causal_top_left),
+        lambda: TC.test_causal_close_to_fp64_masked_attention(200, 333, 128)),
+    "causal_diagonal_key_hidden": (
+        lambda mp: mp.setattr(O, "visible_keys", _causal_strict),
+        TC.test_causal_first_row_is_its_first_value),
     "kv_tile_256": (
         lambda mp: mp.setattr(O, "BKV", 256),
         TA.test_checkpoints_follow_online_softmax_invariants),
