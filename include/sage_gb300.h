@@ -25,7 +25,7 @@
  *    SAGE_ERR_* code when arguments were rejected (nothing enqueued) or the
  *    launch failed.  Errors found on the device (a bounded wait that ran out)
  *    are recorded in a device status word read by sage_get_device_status.
- *  - Only D = 128 is supported.  Q, K, V and O are BF16.
+ *  - Head dimension D = 64 or 128.  Q, K, V and O are BF16.
  */
 #ifndef SAGE_GB300_H
 #define SAGE_GB300_H
@@ -40,7 +40,7 @@ extern "C" {
 enum sage_status {
     SAGE_OK = 0,
     SAGE_ERR_ARG = -1,          /* null pointer, non-positive size, bad length */
-    SAGE_ERR_UNSUPPORTED = -2,  /* D != 128, misaligned pointer or stride */
+    SAGE_ERR_UNSUPPORTED = -2,  /* D not 64 or 128, misaligned pointer or stride */
     SAGE_ERR_LAUNCH = -3,       /* CUDA reported an error at launch */
     SAGE_ERR_TIMEOUT = -4,      /* device: a bounded wait inside a kernel ran out */
     SAGE_ERR_DRIVER = -5,       /* driver entry point for TMA descriptors missing */
@@ -123,6 +123,19 @@ int sage_attn_fwd(const sage_prep_buffers* in, const sage_tensor* o,
                   int B, int H, int Nq, int Nkv, int D,
                   const int32_t* q_len, const int32_t* kv_len,
                   float sm_scale, void* stream);
+
+/* Causal form of sage_attn_fwd (the pages describe only the non-causal
+ * path; this is the same contract with a mask).  Query i of batch item b sees
+ * key j iff j <= i + (kv_len[b] - q_len[b]): the diagonal runs through the
+ * last query and the last key, so j <= i when the lengths are equal.  Rows
+ * that see no key are written as zero.  Arguments, layouts, ownership and
+ * errors are those of sage_attn_fwd.  Each query tile reads only the KV
+ * tiles up to its diagonal; hidden keys inside a tile are masked, and a row's
+ * result equals the non-causal result over the keys it sees. */
+int sage_attn_fwd_causal(const sage_prep_buffers* in, const sage_tensor* o,
+                         int B, int H, int Nq, int Nkv, int D,
+                         const int32_t* q_len, const int32_t* kv_len,
+                         float sm_scale, void* stream);
 
 /* The "QK" checkpoint: exact integer scores S[b,h,i,j] = sum_d q8*k8 from the
  * same tensor-core path sage_attn_fwd uses, written as int32 to

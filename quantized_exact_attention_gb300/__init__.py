@@ -26,9 +26,10 @@ SAGE_ERR_DRIVER = -5
 SAGE_ERR_SCRATCH = -6
 
 D_HEAD = 128
+HEAD_DIMS = (64, 128)       # head dimensions the kernels are built for
 
 # Names the header declares (checked by the CPU tests against the .so exports).
-EXPORTED = ("sage_buffer_sizes", "sage_prep_qkv", "sage_attn_fwd", "sage_qk_int32",
+EXPORTED = ("sage_buffer_sizes", "sage_prep_qkv", "sage_attn_fwd", "sage_attn_fwd_causal", "sage_qk_int32",
             "sage_attention_host", "sage_get_device_status", "sage_status_string",
             "sage_last_launch_count", "sage_debug_inject_fault", "sage_prep_qkv_noalloc",
             "sage_prep_noalloc_capacity")
@@ -80,6 +81,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sage_prep_qkv.argtypes = [P(sage_tensor), P(sage_tensor), P(sage_tensor), i, i, i, i, i, vp, vp,
                                   P(sage_prep_buffers), vp]
     lib.sage_attn_fwd.argtypes = [P(sage_prep_buffers), P(sage_tensor), i, i, i, i, i, vp, vp, f, vp]
+    lib.sage_attn_fwd_causal.argtypes = lib.sage_attn_fwd.argtypes
     lib.sage_qk_int32.argtypes = [P(sage_prep_buffers), vp, i, i, i, i, i, vp, vp, vp]
     lib.sage_attention_host.argtypes = [P(sage_copy), i, P(sage_tensor), P(sage_tensor), P(sage_tensor),
                                         P(sage_prep_buffers), P(sage_tensor), P(sage_copy),
@@ -199,14 +201,18 @@ def sage_prep_noalloc_capacity() -> int:
 
 
 def sage_attn_fwd(bufs: PrepBuffers, o, q_len=None, kv_len=None, sm_scale: float = 0.0, stream=None,
-                  Nkv: int | None = None):
-    """Enqueue the fused attention kernel; o is a [B,H,Nq,D] BF16 view."""
+                  Nkv: int | None = None, causal: bool = False):
+    """Enqueue the fused attention kernel; o is a [B,H,Nq,D] BF16 view.
+    causal=True calls sage_attn_fwd_causal (key j visible to query i iff
+    j <= i + kv_len - q_len)."""
     B, H, Nq, D = o.shape
     Nkv = bufs.k16.shape[2] if Nkv is None else Nkv
     os_, pb = tensor_desc(o), bufs.c_struct()
-    rc = load_library().sage_attn_fwd(ctypes.byref(pb), ctypes.byref(os_), B, H, Nq, Nkv, D,
-                                      _lens(q_len), _lens(kv_len), float(sm_scale), _stream_ptr(stream))
-    _check(rc, "sage_attn_fwd")
+    lib = load_library()
+    fn = lib.sage_attn_fwd_causal if causal else lib.sage_attn_fwd
+    rc = fn(ctypes.byref(pb), ctypes.byref(os_), B, H, Nq, Nkv, D,
+            _lens(q_len), _lens(kv_len), float(sm_scale), _stream_ptr(stream))
+    _check(rc, "sage_attn_fwd_causal" if causal else "sage_attn_fwd")
 
 
 def sage_qk_int32(bufs: PrepBuffers, s: torch.Tensor, q_len=None, kv_len=None, stream=None):
@@ -214,7 +220,7 @@ def sage_qk_int32(bufs: PrepBuffers, s: torch.Tensor, q_len=None, kv_len=None, s
     B, H, Nq, Nkv = s.shape
     assert s.dtype == torch.int32 and s.is_contiguous()
     pb = bufs.c_struct()
-    rc = load_library().sage_qk_int32(ctypes.byref(pb), s.data_ptr(), B, H, Nq, Nkv, D_HEAD,
+    rc = load_library().sage_qk_int32(ctypes.byref(pb), s.data_ptr(), B, H, Nq, Nkv, bufs.q16.shape[3],
                                       _lens(q_len), _lens(kv_len), _stream_ptr(stream))
     _check(rc, "sage_qk_int32")
 
@@ -255,13 +261,13 @@ def sage_debug_inject_fault(mode: int):
 
 
 def attention(q, k, v, q_len=None, kv_len=None, sm_scale: float = 0.0, out=None, int8_codes=False,
-              stream=None):
+              stream=None, causal: bool = False):
     """Prep + fused attention on [B,H,N,D] BF16 CUDA views; returns (o, bufs)."""
     B, H, Nq, D = q.shape
     Nkv = k.shape[2]
-    bufs = alloc_prep_buffers(B, H, Nq, Nkv, q.device, int8_codes=int8_codes)
+    bufs = alloc_prep_buffers(B, H, Nq, Nkv, q.device, int8_codes=int8_codes, D=D)
     if out is None:
         out = torch.zeros((B, Nq, H, D), dtype=torch.bfloat16, device=q.device).permute(0, 2, 1, 3)
     sage_prep_qkv(q, k, v, bufs, q_len, kv_len, stream)
-    sage_attn_fwd(bufs, out, q_len, kv_len, sm_scale, stream, Nkv=Nkv)
+    sage_attn_fwd(bufs, out, q_len, kv_len, sm_scale, stream, Nkv=Nkv, causal=causal)
     return out, bufs

@@ -60,7 +60,7 @@ bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, void* base, uint64_t x, u
 int check_shape(int B, int H, int Nq, int Nkv, int D) {
     if (B <= 0 || H <= 0 || Nq <= 0 || Nkv <= 0) return SAGE_ERR_ARG;
     if (B > 65535 || H > 65535 || Nq > (1 << 24) || Nkv > (1 << 24)) return SAGE_ERR_ARG;
-    if (D != kD) return SAGE_ERR_UNSUPPORTED;
+    if (D != 64 && D != 128) return SAGE_ERR_UNSUPPORTED;
     return SAGE_OK;
 }
 
@@ -118,17 +118,17 @@ int sage_buffer_sizes(int B, int H, int Nq, int Nkv, int D, sage_sizes* out) {
     const int64_t bh = (int64_t)B * H;
     const int64_t pad = nkv_pad_of(Nkv);
     const int64_t nchunks = ceil_div(Nkv, kMeanChunk);
-    out->q16 = (size_t)(bh * Nq * kD * 2);
-    out->k16 = (size_t)(bh * Nkv * kD * 2);
-    out->v8t = (size_t)(bh * kD * pad);
+    out->q16 = (size_t)(bh * Nq * D * 2);
+    out->k16 = (size_t)(bh * Nkv * D * 2);
+    out->v8t = (size_t)(bh * D * pad);
     out->q_scale = (size_t)(bh * ceil_div(Nq, kBQS) * 4);
     out->k_scale = (size_t)(bh * ceil_div(Nkv, kBKS) * 4);
-    out->v_scale = (size_t)(bh * kD * 4);
-    out->k_mean = (size_t)(bh * kD * 4);
-    out->q8 = (size_t)(bh * Nq * kD);
-    out->k8 = (size_t)(bh * Nkv * kD);
+    out->v_scale = (size_t)(bh * D * 4);
+    out->k_mean = (size_t)(bh * D * 4);
+    out->q8 = (size_t)(bh * Nq * D);
+    out->k8 = (size_t)(bh * Nkv * D);
     // partial sums + partial amax [B,H,chunks,D] and the V inverse scales [B,H,D]
-    out->workspace = (size_t)(2 * bh * nchunks * kD * 4 + bh * kD * 4);
+    out->workspace = (size_t)(2 * bh * nchunks * D * 4 + bh * D * 4);
     out->nkv_pad = pad;
     return SAGE_OK;
 }
@@ -151,7 +151,7 @@ int sage_prep_qkv(const sage_tensor* q, const sage_tensor* k, const sage_tensor*
     p.qsb = q->stride_b; p.qsh = q->stride_h; p.qsn = q->stride_n;
     p.ksb = k->stride_b; p.ksh = k->stride_h; p.ksn = k->stride_n;
     p.vsb = v->stride_b; p.vsh = v->stride_h; p.vsn = v->stride_n;
-    p.B = B; p.H = H; p.Nq = Nq; p.Nkv = Nkv;
+    p.B = B; p.H = H; p.Nq = Nq; p.Nkv = Nkv; p.D = D;
     p.nkv_pad = (int)sz.nkv_pad;
     p.nq_blocks = (int)ceil_div(Nq, kBQS);
     p.nk_blocks = (int)ceil_div(Nkv, kBKS);
@@ -161,7 +161,7 @@ int sage_prep_qkv(const sage_tensor* q, const sage_tensor* k, const sage_tensor*
     p.q8 = out->q8; p.k8 = out->k8;
     p.q_scale = out->q_scale; p.k_scale = out->k_scale; p.v_scale = out->v_scale; p.k_mean = out->k_mean;
     float* ws = static_cast<float*>(out->workspace);
-    const int64_t part = (int64_t)B * H * p.n_chunks * kD;
+    const int64_t part = (int64_t)B * H * p.n_chunks * D;
     p.psum = ws;
     p.pamax = ws + part;
     p.v_inv = ws + 2 * part;
@@ -173,7 +173,7 @@ int sage_prep_qkv(const sage_tensor* q, const sage_tensor* k, const sage_tensor*
 
 static int attn_common(const sage_prep_buffers* in, const sage_tensor* o, int32_t* s_out, int B, int H, int Nq,
                        int Nkv, int D, const int32_t* q_len, const int32_t* kv_len, float sm_scale,
-                       void* stream, bool capture) {
+                       void* stream, bool capture, bool causal) {
     int rc = check_shape(B, H, Nq, Nkv, D);
     if (rc != SAGE_OK) return rc;
     sage_sizes sz;
@@ -189,12 +189,15 @@ static int attn_common(const sage_prep_buffers* in, const sage_tensor* o, int32_
 
     const uint64_t bh = (uint64_t)B * H;
     CUtensorMap tq, tk, tv;
-    if (!encode_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, in->q16, kD, (uint64_t)Nq, bh, kD * 2,
-                   (uint64_t)Nq * kD * 2, 64, 128) ||
-        !encode_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, in->k16, kD, (uint64_t)Nkv, bh, kD * 2,
-                   (uint64_t)Nkv * kD * 2, 64, 128) ||
-        !encode_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, in->v8t, (uint64_t)sz.nkv_pad, kD, bh,
-                   (uint64_t)sz.nkv_pad, (uint64_t)sz.nkv_pad * kD, 128, 128))
+    // Q/K code images: boxes of 64 channels (128 bytes, one swizzle row) x 128
+    // rows; V^T: boxes of 128 tokens x D channels.
+    const uint64_t d = (uint64_t)D;
+    if (!encode_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, in->q16, d, (uint64_t)Nq, bh, d * 2,
+                   (uint64_t)Nq * d * 2, 64, 128) ||
+        !encode_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, in->k16, d, (uint64_t)Nkv, bh, d * 2,
+                   (uint64_t)Nkv * d * 2, 64, 128) ||
+        !encode_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, in->v8t, (uint64_t)sz.nkv_pad, d, bh,
+                   (uint64_t)sz.nkv_pad, (uint64_t)sz.nkv_pad * d, 128, (uint32_t)D))
         return encode_fn() ? SAGE_ERR_UNSUPPORTED : SAGE_ERR_DRIVER;
 
     AttnParams p{};
@@ -205,7 +208,7 @@ static int attn_common(const sage_prep_buffers* in, const sage_tensor* o, int32_
         p.osb = o->stride_b; p.osh = o->stride_h; p.osn = o->stride_n;
     }
     p.s_out = s_out;
-    p.B = B; p.H = H; p.Nq = Nq; p.Nkv = Nkv;
+    p.B = B; p.H = H; p.Nq = Nq; p.Nkv = Nkv; p.D = D;
     p.nq_blocks = (int)ceil_div(Nq, kBQS);
     p.nk_blocks = (int)ceil_div(Nkv, kBKS);
     const double scale = sm_scale > 0.f ? (double)sm_scale : 1.0 / std::sqrt((double)D);
@@ -214,19 +217,24 @@ static int attn_common(const sage_prep_buffers* in, const sage_tensor* o, int32_
     p.fault_mode = fault_mode_for_next_launch;
     fault_mode_for_next_launch = 0;
     int launches = 0;
-    rc = status_from(launch_attn(p, tq, tk, tv, capture, static_cast<cudaStream_t>(stream), &launches));
+    rc = status_from(launch_attn(p, tq, tk, tv, capture, causal, static_cast<cudaStream_t>(stream), &launches));
     if (rc == SAGE_OK) g_last_launches = launches;
     return rc;
 }
 
 int sage_attn_fwd(const sage_prep_buffers* in, const sage_tensor* o, int B, int H, int Nq, int Nkv, int D,
                   const int32_t* q_len, const int32_t* kv_len, float sm_scale, void* stream) {
-    return attn_common(in, o, nullptr, B, H, Nq, Nkv, D, q_len, kv_len, sm_scale, stream, false);
+    return attn_common(in, o, nullptr, B, H, Nq, Nkv, D, q_len, kv_len, sm_scale, stream, false, false);
+}
+
+int sage_attn_fwd_causal(const sage_prep_buffers* in, const sage_tensor* o, int B, int H, int Nq, int Nkv, int D,
+                         const int32_t* q_len, const int32_t* kv_len, float sm_scale, void* stream) {
+    return attn_common(in, o, nullptr, B, H, Nq, Nkv, D, q_len, kv_len, sm_scale, stream, false, true);
 }
 
 int sage_qk_int32(const sage_prep_buffers* in, int32_t* s, int B, int H, int Nq, int Nkv, int D,
                   const int32_t* q_len, const int32_t* kv_len, void* stream) {
-    return attn_common(in, nullptr, s, B, H, Nq, Nkv, D, q_len, kv_len, 0.f, stream, true);
+    return attn_common(in, nullptr, s, B, H, Nq, Nkv, D, q_len, kv_len, 0.f, stream, true, false);
 }
 
 int sage_attention_host(const sage_copy* inputs, int n_inputs, const sage_tensor* q, const sage_tensor* k,

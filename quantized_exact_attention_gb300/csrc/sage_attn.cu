@@ -52,16 +52,7 @@ constexpr int kWarpMma = 17;
 constexpr int kNK = 3;              // K ring depth
 constexpr int kNV = 3;              // V ring depth
 constexpr int kNS = 3;              // S/P buffers in tensor memory
-constexpr uint32_t kTileQBytes = 128 * 128 * 2;
-constexpr uint32_t kTileKBytes = 128 * 128 * 2;
-constexpr uint32_t kTileVBytes = 128 * 128;
-constexpr uint32_t kHalfBytes = 128 * 128;      // one 64-column half of an FP16 tile
-
-// shared memory map (offsets from a 1024-byte aligned base)
-constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_K = OFF_Q + kTileQBytes;
-constexpr uint32_t OFF_V = OFF_K + kNK * kTileKBytes;
-constexpr uint32_t OFF_BAR = OFF_V + kNV * kTileVBytes;
+constexpr uint32_t kHalfBytes = 128 * 128;      // 64 FP16 channels (one 128-byte swizzle row) x 128 rows
 
 enum Bar : uint32_t {
     B_QFULL = 0,
@@ -82,17 +73,31 @@ enum Bar : uint32_t {
     B_COUNT = B_DRAIN + 1
 };
 
-constexpr uint32_t OFF_ALPHA = OFF_BAR + ((B_COUNT * 8 + 15) / 16) * 16;   // float [2][128]
-constexpr uint32_t OFF_XM = OFF_ALPHA + 2 * 128 * 4;                       // float [2 buf][2 half][128]
-constexpr uint32_t OFF_L = OFF_XM + 4 * 128 * 4;                           // float [2 half][128]
-constexpr uint32_t OFF_VS = OFF_L + 2 * 128 * 4;                           // float [128]
-constexpr uint32_t OFF_TMEM = OFF_VS + 128 * 4;                            // u32
-constexpr uint32_t OFF_ABORT = OFF_TMEM + 16;                              // int
-constexpr uint32_t kSmemUsed = OFF_ABORT + 16;
-constexpr uint32_t kSmemBytes = kSmemUsed + 1024;                          // + alignment slack
+// Shared-memory map for head dimension D (offsets from a 1024-byte aligned
+// base).  Q and K tiles hold 128 rows of FP16 codes as D/64 column blocks of
+// kHalfBytes; a V tile holds D channel rows of 128 e4m3 tokens.
+template <int D>
+struct Smem {
+    static_assert(D == 64 || D == 128, "head dimension");
+    static constexpr uint32_t kTileQBytes = 128 * D * 2;
+    static constexpr uint32_t kTileKBytes = 128 * D * 2;
+    static constexpr uint32_t kTileVBytes = 128 * D;
+    static constexpr uint32_t OFF_Q = 0;
+    static constexpr uint32_t OFF_K = OFF_Q + kTileQBytes;
+    static constexpr uint32_t OFF_V = OFF_K + kNK * kTileKBytes;
+    static constexpr uint32_t OFF_BAR = OFF_V + kNV * kTileVBytes;
+    static constexpr uint32_t OFF_ALPHA = OFF_BAR + ((B_COUNT * 8 + 15) / 16) * 16;   // float [2][128]
+    static constexpr uint32_t OFF_XM = OFF_ALPHA + 2 * 128 * 4;                       // float [2 buf][2 half][128]
+    static constexpr uint32_t OFF_L = OFF_XM + 4 * 128 * 4;                           // float [2 half][128]
+    static constexpr uint32_t OFF_VS = OFF_L + 2 * 128 * 4;                           // float [D]
+    static constexpr uint32_t OFF_TMEM = OFF_VS + 128 * 4;                            // u32
+    static constexpr uint32_t OFF_ABORT = OFF_TMEM + 16;                              // int
+    static constexpr uint32_t kSmemUsed = OFF_ABORT + 16;
+    static constexpr uint32_t kSmemBytes = kSmemUsed + 1024;                          // + alignment slack
+};
 
 constexpr uint32_t TM_S = 0;        // S buffer b (0..2) at column 128*b
-constexpr uint32_t TM_PV = 384;     // PV buffer (FP16 tile sums, one per column)
+constexpr uint32_t TM_PV = 384;     // PV buffer (D FP16 tile sums, one per column)
 // P of tile t is written over the first 32 columns of S buffer t%2 once both
 // halves of every row have read their S values; the next QK into that buffer
 // is issued after the PV MMA that reads P, and tcgen05.mma executes in issue
@@ -129,10 +134,19 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
     return lo | (hi << 16);
 }
 
-template <bool kCapture>
+// kCausal: key j is visible to query i iff j <= i + (Lk - Lq); a CTA visits
+// only the KV tiles up to the diagonal of its last row, and rows that see no
+// key are written as zero.
+template <int D, bool kCapture, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
 sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
+    using L = Smem<D>;
+    constexpr uint32_t kTileQBytes = L::kTileQBytes, kTileKBytes = L::kTileKBytes, kTileVBytes = L::kTileVBytes;
+    constexpr uint32_t OFF_Q = L::OFF_Q, OFF_K = L::OFF_K, OFF_V = L::OFF_V, OFF_BAR = L::OFF_BAR;
+    constexpr uint32_t OFF_ALPHA = L::OFF_ALPHA, OFF_XM = L::OFF_XM, OFF_L = L::OFF_L, OFF_VS = L::OFF_VS;
+    constexpr uint32_t OFF_TMEM = L::OFF_TMEM, OFF_ABORT = L::OFF_ABORT;
+    constexpr int kDH = D / 2;                              // output channels per correction thread
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_u32(smem_raw);
     const uint32_t sbase = (raw_base + 1023u) & ~1023u;
@@ -140,25 +154,30 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int qtile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    // causal: the longest query tiles start first
+    const int qtile = kCausal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+    const int h = blockIdx.y, b = blockIdx.z;
     const int bh = b * p.H + h;
     const int q0 = qtile * 128;
     const int lq = clamp_len(p.q_len, b, p.Nq);
     const int lk = clamp_len(p.kv_len, b, p.Nkv);
     if (q0 >= lq) return;                                   // no valid row in this tile
+    const int diag = lk - lq;                               // causal: row i sees keys j <= i + diag
+    // keys any row of this tile can see
+    const int kv_end = kCausal ? min(lk, min(q0 + 127, lq - 1) + diag + 1) : lk;
 
-    if (lk == 0) {                                          // no keys: rows are zero
+    if (kv_end <= 0) {                                      // no keys: rows are zero
         if (!kCapture && threadIdx.x < 128) {
             const int r = q0 + threadIdx.x;
             if (r < lq) {
                 uint4* dst = reinterpret_cast<uint4*>(p.o + b * p.osb + h * p.osh + (int64_t)r * p.osn);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+                for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
             }
         }
         return;
     }
-    const int T = (lk + 127) / 128;                         // KV tiles
+    const int T = (kv_end + 127) / 128;                     // KV tiles
 
     auto bar = [&](uint32_t i) -> uint32_t { return sbase + OFF_BAR + 8u * i; };
     float* alpha_s = reinterpret_cast<float*>(sgen + OFF_ALPHA);
@@ -233,7 +252,9 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(bar(B_SFREE + s3));
-            const int lim = lk - t * 128 - half * 64;       // valid columns of this half (may be <= 0)
+            // valid columns of this half (may be <= 0); causal: per row
+            const int lim = (kCausal ? min(lk, q0 + row + diag + 1) : lk) - t * 128 - half * 64;
+            const bool full = kCausal ? __all_sync(0xffffffffu, lim >= 64) : (lim >= 64);
 
             if (kCapture) {
                 const int r = q0 + row;
@@ -250,7 +271,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
             // half-row maximum of the raw integer scores
             float mx;
-            if (lim >= 64) {
+            if (full) {
                 float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
 #pragma unroll
                 for (int i = 0; i < 32; i += 4) {
@@ -282,7 +303,10 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 break;
             }
             tc_fence_after();
-            const float m_new = fmaxf(m_run, fmaxf(xm[(sb * 2 + 0) * 128 + row], xm[(sb * 2 + 1) * 128 + row]));
+            float m_new = fmaxf(m_run, fmaxf(xm[(sb * 2 + 0) * 128 + row], xm[(sb * 2 + 1) * 128 + row]));
+            // causal: a row that has seen no key yet keeps m = -inf; measure from
+            // 0 so that alpha = 0 and every p = 0 instead of NaN
+            if (kCausal && m_new == -INFINITY) m_new = 0.f;
             const float alpha = ex2_approx(m_run - m_new);  // first tile: 2^-inf = 0
             const float nb = kLog2SP - m_new;               // P is produced pre-scaled by 448
 
@@ -303,7 +327,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 add2(sb0, sb1, e2, e3);
                 pk[col >> 2] = pack_e4m3x4(e0, e1, e2, e3);
             };
-            if (lim >= 64) {
+            if (full) {
 #pragma unroll
                 for (int i = 0; i < 32; i += 4) { quad(s0, i, i, false); quad(s1, i, i + 32, false); }
             } else {
@@ -326,7 +350,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             mbar_arrive(bar(B_PFULL + s3));
             if (half == 0) mbar_arrive(bar(B_AFULL + sb));
             l_run = fmaf(l_run, alpha, tile_sum);
-            m_run = m_new;
+            m_run = (kCausal && l_run == 0.f) ? -INFINITY : m_new;
         }
         if (!kCapture && ok) {
             l_s[half * 128 + row] = l_run;
@@ -338,11 +362,11 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const int quarter = (warp - 8) & 3, half = (warp - 8) >> 2;
             const int row = quarter * 32 + lane;
             const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-            if (half == 0) vs_s[row] = p.v_scale[(int64_t)bh * kD + row];
+            if (half == 0 && row < D) vs_s[row] = p.v_scale[(int64_t)bh * D + row];
             named_bar_sync(5, 256);
-            float ro[64];
+            float ro[kDH];
 #pragma unroll
-            for (int i = 0; i < 64; ++i) ro[i] = 0.f;
+            for (int i = 0; i < kDH; ++i) ro[i] = 0.f;
             bool ok = true;
             for (int t = 0; t < T; ++t) {
                 const int sb = t & 1;
@@ -361,11 +385,11 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 }
                 tc_fence_after();
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                for (int c = 0; c < kDH / 32; ++c) {
                     uint32_t v[16];                         // FP16 tile sums, two per register
-                    tmem_ld32_pack16(tmem + lane_base + TM_PV + half * 64 + c * 32, v);
+                    tmem_ld32_pack16(tmem + lane_base + TM_PV + half * kDH + c * 32, v);
                     tmem_wait_ld();
-                    if (c == 1) {
+                    if (c == kDH / 32 - 1) {
                         tc_fence_before();
                         mbar_arrive(bar(B_PVFREE));
                     }
@@ -381,19 +405,21 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
             if (ok && warp_wait(bar(B_LFULL), 0, abort_flag)) {
                 // l carries the 448 scale of P, so (RO / l) * v_scale is the output
-                const float rl = __frcp_rn(l_s[row] + l_s[128 + row]);
+                const float l_row = l_s[row] + l_s[128 + row];
+                // causal rows that saw no key have l = 0 and RO = 0: write zeros
+                const float rl = (kCausal && l_row == 0.f) ? 0.f : __frcp_rn(l_row);
                 const int r = q0 + row;
                 if (r < lq) {
                     uint4* dst = reinterpret_cast<uint4*>(p.o + b * p.osb + h * p.osh + (int64_t)r * p.osn +
-                                                          half * 64);
+                                                          half * kDH);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
+                    for (int i = 0; i < kDH / 8; ++i) {
                         uint32_t w[4];
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             const int d = i * 8 + j * 2;
-                            const float o0 = __fmul_rn(__fmul_rn(ro[d], rl), vs_s[half * 64 + d]);
-                            const float o1 = __fmul_rn(__fmul_rn(ro[d + 1], rl), vs_s[half * 64 + d + 1]);
+                            const float o0 = __fmul_rn(__fmul_rn(ro[d], rl), vs_s[half * kDH + d]);
+                            const float o1 = __fmul_rn(__fmul_rn(ro[d + 1], rl), vs_s[half * kDH + d + 1]);
                             const __nv_bfloat162 pr = __floats2bfloat162_rn(o0, o1);
                             w[j] = *reinterpret_cast<const uint32_t*>(&pr);
                         }
@@ -413,15 +439,16 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             for (int i = 0; i < kNV; ++i) last_v[i] = -1;
             bool ok = true;
             mbar_arrive_expect_tx(bar(B_QFULL), kTileQBytes);
-            tma_load_3d(sQ, &tm_q, 0, q0, bh, bar(B_QFULL));
-            tma_load_3d(sQ + kHalfBytes, &tm_q, 64, q0, bh, bar(B_QFULL));
+#pragma unroll
+            for (int hh = 0; hh < D / 64; ++hh) tma_load_3d(sQ + hh * kHalfBytes, &tm_q, hh * 64, q0, bh, bar(B_QFULL));
             auto load_k = [&](int t) -> bool {
                 const int st = t % kNK;
                 if (t >= kNK && !mbar_wait(bar(B_KEMPTY + st), ((t / kNK) - 1) & 1, abort_flag)) return false;
                 const uint32_t dst = sbase + OFF_K + st * kTileKBytes;
                 mbar_arrive_expect_tx(bar(B_KFULL + st), kTileKBytes);
-                tma_load_3d(dst, &tm_k, 0, t * 128, bh, bar(B_KFULL + st));
-                tma_load_3d(dst + kHalfBytes, &tm_k, 64, t * 128, bh, bar(B_KFULL + st));
+#pragma unroll
+                for (int hh = 0; hh < D / 64; ++hh)
+                    tma_load_3d(dst + hh * kHalfBytes, &tm_k, hh * 64, t * 128, bh, bar(B_KFULL + st));
                 last_k[st] = t;
                 return true;
             };
@@ -458,7 +485,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // ===================================================== MMA issuer
         if (lane == 0) {
             constexpr uint32_t kIdescQK = idesc_f32acc(0u, 128u, 128u);   // F16 x F16 -> F32
-            constexpr uint32_t kIdescPV = idesc_f16acc(0u, 128u, 128u);   // E4M3 x E4M3 -> F16
+            constexpr uint32_t kIdescPV = idesc_f16acc(0u, 128u, (uint32_t)D);   // E4M3 x E4M3 -> F16
             const uint32_t sQ = sbase + OFF_Q;
             bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag);
             int fail_tile = 0;
@@ -481,7 +508,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 const uint64_t bK = dK + (uint64_t)(k_st * (kTileKBytes >> 4));
                 const uint32_t dS = tmem + TM_S + qb * 128;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
+                for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
                     mma_f16_ss(dS, dQ + off, bK + off, kIdescQK, kk > 0 ? 1u : 0u);
                 }
@@ -533,31 +560,40 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
 }
 
-bool g_attr_set[2][64] = {};
-
-template <bool kCapture>
+template <int D, bool kCapture, bool kCausal>
 cudaError_t launch_one(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, cudaStream_t s) {
+    static bool attr_set[64] = {};                          // per device, per instantiation
+    constexpr uint32_t kSmemBytes = Smem<D>::kSmemBytes;
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!g_attr_set[kCapture ? 1 : 0][dev]) {
-        cudaError_t e = cudaFuncSetAttribute(sage_attn_kernel<kCapture>,
+    if (!attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(sage_attn_kernel<D, kCapture, kCausal>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e != cudaSuccess) return e;
-        g_attr_set[kCapture ? 1 : 0][dev] = true;
+        attr_set[dev] = true;
     }
     dim3 grid((unsigned)((p.Nq + 127) / 128), (unsigned)p.H, (unsigned)p.B);
-    sage_attn_kernel<kCapture><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+    sage_attn_kernel<D, kCapture, kCausal><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
     return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                     bool capture, bool causal, cudaStream_t s) {
+    if (capture) return launch_one<D, true, false>(p, tq, tk, tv, s);
+    return causal ? launch_one<D, false, true>(p, tq, tk, tv, s) : launch_one<D, false, false>(p, tq, tk, tv, s);
 }
 
 }  // namespace
 
 cudaError_t launch_attn(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                        const CUtensorMap& tv, bool capture, cudaStream_t s, int* launches) {
+                        const CUtensorMap& tv, bool capture, bool causal, cudaStream_t s, int* launches) {
     *launches = 1;
-    return capture ? launch_one<true>(p, tq, tk, tv, s) : launch_one<false>(p, tq, tk, tv, s);
+    if (p.D == 128) return launch_d<128>(p, tq, tk, tv, capture, causal, s);
+    if (p.D == 64) return launch_d<64>(p, tq, tk, tv, capture, causal, s);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace sage

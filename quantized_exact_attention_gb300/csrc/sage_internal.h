@@ -10,7 +10,6 @@ namespace sage {
 
 // Contract tile constants.  The pages name the stages but give no numbers;
 // these are the readings the whole library is built on.
-constexpr int kD = 128;          // head dimension (Q128 x KV192 x D128 prototype shape)
 constexpr int kBQS = 128;        // rows per INT8 Q scale block (one 128-row query tile)
 constexpr int kBKS = 64;         // rows per INT8 K scale block (64-key K/V slots)
 constexpr int kBKV = 128;        // keys per online-softmax tile and per inner PV sum
@@ -26,7 +25,7 @@ struct PrepParams {
     const uint16_t* k;
     const uint16_t* v;
     int64_t qsb, qsh, qsn, ksb, ksh, ksn, vsb, vsh, vsn;   // element strides
-    int B, H, Nq, Nkv, nkv_pad;
+    int B, H, Nq, Nkv, D, nkv_pad;         // D: head dimension, 64 or 128
     int nq_blocks, nk_blocks, n_chunks;    // ceil(Nq/128), ceil(Nkv/64), ceil(Nkv/64)
     const int32_t* q_len;                  // device [B] or null
     const int32_t* kv_len;
@@ -53,7 +52,7 @@ struct AttnParams {
     uint16_t* o;                           // BF16 bit patterns
     int64_t osb, osh, osn;
     int32_t* s_out;                        // QK checkpoint output (capture kernel only)
-    int B, H, Nq, Nkv;
+    int B, H, Nq, Nkv, D;                  // D: head dimension, 64 or 128
     int nq_blocks, nk_blocks;
     float c;                               // fp32(sm_scale * log2(e))
     int* status;                           // device status words
@@ -67,6 +66,6 @@ int* device_status_ptr();                  // per-device address of the status w
 
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t s, int* launches);
 cudaError_t launch_attn(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                        const CUtensorMap& tv, bool capture, cudaStream_t s, int* launches);
+                        const CUtensorMap& tv, bool capture, bool causal, cudaStream_t s, int* launches);
 
 }  // namespace sage

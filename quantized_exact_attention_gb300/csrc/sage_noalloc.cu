@@ -92,7 +92,7 @@ extern "C" int sage_prep_qkv_noalloc(const sage_tensor* q, const sage_tensor* k,
     p.qsb = q->stride_b; p.qsh = q->stride_h; p.qsn = q->stride_n;
     p.ksb = k->stride_b; p.ksh = k->stride_h; p.ksn = k->stride_n;
     p.vsb = v->stride_b; p.vsh = v->stride_h; p.vsn = v->stride_n;
-    p.B = B; p.H = H; p.Nq = Nq; p.Nkv = Nkv;
+    p.B = B; p.H = H; p.Nq = Nq; p.Nkv = Nkv; p.D = D;
     p.nkv_pad = (int)sz.nkv_pad;
     p.nq_blocks = (int)ceil_div(Nq, kBQS);
     p.nk_blocks = (int)ceil_div(Nkv, kBKS);
@@ -101,7 +101,7 @@ extern "C" int sage_prep_qkv_noalloc(const sage_tensor* q, const sage_tensor* k,
     p.q16 = out->q16; p.k16 = out->k16; p.v8t = out->v8t;
     p.q8 = out->q8; p.k8 = out->k8;
     p.q_scale = out->q_scale; p.k_scale = out->k_scale; p.v_scale = out->v_scale; p.k_mean = out->k_mean;
-    const int64_t part = (int64_t)B * H * p.n_chunks * kD;
+    const int64_t part = (int64_t)B * H * p.n_chunks * D;
     p.psum = scratch;
     p.pamax = scratch + part;
     p.v_inv = scratch + 2 * part;

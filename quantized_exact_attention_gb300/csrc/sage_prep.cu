@@ -12,7 +12,9 @@
 //                     written transposed: token index fastest)
 // Loaded BF16 data stays packed in registers (8 values per 16-byte word) and
 // is widened on use, which keeps register use low enough for several blocks
-// per SM and enough bytes in flight to stream HBM.
+// per SM and enough bytes in flight to stream HBM.  Every kernel is
+// instantiated for head dimensions 64 and 128: a thread owns 8 channels, so a
+// row takes D/8 threads and the 256 threads of a block cover 2048/D rows.
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
@@ -21,7 +23,19 @@
 namespace sage {
 namespace {
 
-constexpr int kStatChunksPerBlock = 16;   // 16 chunks x 16 channel groups = 256 threads
+// Thread layout for head dimension D (256 threads per block, 8 channels each).
+template <int D>
+struct PrepShape {
+    static_assert(D == 64 || D == 128, "head dimension");
+    static constexpr int kGroups = D / 8;                 // threads per row
+    static constexpr int kRowsPerPass = 256 / kGroups;    // rows a block covers at once
+    static constexpr int kStatChunks = kRowsPerPass;      // 64-token chunks per statistics block
+    static constexpr int kQPasses = kBQS / kRowsPerPass;  // passes over a 128-row Q block
+    static constexpr int kKPasses = kBKS / kRowsPerPass;  // passes over a 64-row K block
+    static constexpr int kVTokens = 8192 / D;             // tokens per V tile (64 or 128)
+    static constexpr int kTokGroups = kVTokens / 4;       // threads per channel group, 4 tokens each
+    static constexpr int kVStride = kTokGroups + 4;       // words per transposed row (+4 pad)
+};
 
 __device__ __forceinline__ int clamp_len(const int32_t* lens, int b, int n) {
     if (lens == nullptr) return n;
@@ -100,8 +114,9 @@ __device__ __forceinline__ void store_row_codes(const int (&c)[8], uint16_t* img
 // Statistics: thread (chunk slot cl, channel group dg) owns 8 channels of one
 // 64-token chunk and walks its tokens in ascending order, so every partial
 // sum is the FP32 left-to-right sum the contract pins.
+template <int D>
 __device__ __forceinline__ void chunk_stats(const PrepParams& p, int b, int h, int c) {
-    const int dg = threadIdx.x & 15;
+    const int dg = threadIdx.x % PrepShape<D>::kGroups;
     const int lk = clamp_len(p.kv_len, b, p.Nkv);
     const int d0 = dg * 8;
     const int t0 = c * kMeanChunk;
@@ -141,7 +156,7 @@ __device__ __forceinline__ void chunk_stats(const PrepParams& p, int b, int h, i
             a[i] = fmaxf(a[i], fabsf(vx[i]));
         }
     }
-    const int64_t o = (((int64_t)b * p.H + h) * p.n_chunks + c) * kD + d0;
+    const int64_t o = (((int64_t)b * p.H + h) * p.n_chunks + c) * D + d0;
     float4* ps = reinterpret_cast<float4*>(p.psum + o);
     float4* pa = reinterpret_cast<float4*>(p.pamax + o);
     ps[0] = make_float4(s[0], s[1], s[2], s[3]);
@@ -151,47 +166,51 @@ __device__ __forceinline__ void chunk_stats(const PrepParams& p, int b, int h, i
 }
 
 // Q block: rows [r0, r0+128), one INT8 scale for the whole block.
+template <int D>
 __device__ __forceinline__ void quant_q_block(const PrepParams& p, int b, int h, int qb, float* red) {
+    using Sh = PrepShape<D>;
     const int bh = b * p.H + h;
     const int tid = threadIdx.x;
     const int lq = clamp_len(p.q_len, b, p.Nq);
-    const int dg = tid & 15, rs = tid >> 4;
+    const int dg = tid % Sh::kGroups, rs = tid / Sh::kGroups;
     const int d0 = dg * 8, r0 = qb * kBQS;
-    uint4 xr[8];
+    uint4 xr[Sh::kQPasses];
     float amax = 0.f;
     const uint16_t* qp = p.q + b * p.qsb + h * p.qsh + d0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int r = r0 + rs + 16 * i;
+    for (int i = 0; i < Sh::kQPasses; ++i) {
+        const int r = r0 + rs + Sh::kRowsPerPass * i;
         xr[i] = (r < lq) ? ldg16(qp + (int64_t)r * p.qsn) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) amax = absmax8(xr[i], amax);
+    for (int i = 0; i < Sh::kQPasses; ++i) amax = absmax8(xr[i], amax);
     amax = block_max_256(amax, red);
     const float inv = amax > 0.f ? __fdiv_rn(127.0f, amax) : 0.f;
     if (tid == 0) p.q_scale[(int64_t)bh * p.nq_blocks + qb] = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int r = r0 + rs + 16 * i;
+    for (int i = 0; i < Sh::kQPasses; ++i) {
+        const int r = r0 + rs + Sh::kRowsPerPass * i;
         if (r >= p.Nq) continue;
         float x[8];
         unpack8(xr[i], x);
         int c[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) c[e] = (r < lq) ? int8_code(x[e], inv) : 0;
-        store_row_codes(c, p.q16, p.q8, ((int64_t)bh * p.Nq + r) * kD + d0);
+        store_row_codes(c, p.q16, p.q8, ((int64_t)bh * p.Nq + r) * D + d0);
     }
 }
 
+template <int D>
 __global__ void __launch_bounds__(256, 3) prep_stats_q_kernel(const PrepParams p) {
+    using Sh = PrepShape<D>;
     __shared__ float red[8];
     const int b = blockIdx.z, h = blockIdx.y;
-    const int n_stat_blocks = (p.n_chunks + kStatChunksPerBlock - 1) / kStatChunksPerBlock;
+    const int n_stat_blocks = (p.n_chunks + Sh::kStatChunks - 1) / Sh::kStatChunks;
     if ((int)blockIdx.x < n_stat_blocks) {
-        const int c = blockIdx.x * kStatChunksPerBlock + (threadIdx.x >> 4);
-        if (c < p.n_chunks) chunk_stats(p, b, h, c);
+        const int c = blockIdx.x * Sh::kStatChunks + (threadIdx.x / Sh::kGroups);
+        if (c < p.n_chunks) chunk_stats<D>(p, b, h, c);
     } else {
-        quant_q_block(p, b, h, blockIdx.x - n_stat_blocks, red);
+        quant_q_block<D>(p, b, h, blockIdx.x - n_stat_blocks, red);
     }
 }
 
@@ -200,11 +219,12 @@ __global__ void __launch_bounds__(256, 3) prep_stats_q_kernel(const PrepParams p
 // fetched 32 at a time (independent loads in flight) and then added strictly
 // in ascending chunk order.
 // ---------------------------------------------------------------------------
+template <int D>
 __global__ void __launch_bounds__(128) prep_finalize_kernel(const PrepParams p) {
     const int b = blockIdx.y, h = blockIdx.x, d = threadIdx.x;
     const int lk = clamp_len(p.kv_len, b, p.Nkv);
     const int nc = (lk + kMeanChunk - 1) / kMeanChunk;
-    const int64_t base = ((int64_t)b * p.H + h) * p.n_chunks * kD + d;
+    const int64_t base = ((int64_t)b * p.H + h) * p.n_chunks * D + d;
     const float* ps = p.psum + base;
     const float* pa = p.pamax + base;
     float total = 0.f, amax = 0.f;
@@ -213,8 +233,8 @@ __global__ void __launch_bounds__(128) prep_finalize_kernel(const PrepParams p) 
         float sv[32], av[32];
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
-            sv[u] = ps[(int64_t)(c + u) * kD];
-            av[u] = pa[(int64_t)(c + u) * kD];
+            sv[u] = ps[(int64_t)(c + u) * D];
+            av[u] = pa[(int64_t)(c + u) * D];
         }
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
@@ -223,10 +243,10 @@ __global__ void __launch_bounds__(128) prep_finalize_kernel(const PrepParams p) 
         }
     }
     for (; c < nc; ++c) {
-        total = __fadd_rn(total, ps[(int64_t)c * kD]);
-        amax = fmaxf(amax, pa[(int64_t)c * kD]);
+        total = __fadd_rn(total, ps[(int64_t)c * D]);
+        amax = fmaxf(amax, pa[(int64_t)c * D]);
     }
-    const int64_t o = ((int64_t)b * p.H + h) * kD + d;
+    const int64_t o = ((int64_t)b * p.H + h) * D + d;
     p.k_mean[o] = lk > 0 ? __fdiv_rn(total, (float)lk) : 0.f;
     p.v_scale[o] = amax > 0.f ? __fdiv_rn(amax, kSV) : 0.f;
     p.v_inv[o] = amax > 0.f ? __fdiv_rn(kSV, amax) : 0.f;
@@ -237,30 +257,32 @@ __global__ void __launch_bounds__(128) prep_finalize_kernel(const PrepParams p) 
 // then V tiles.  256 threads.
 // ---------------------------------------------------------------------------
 // K block: rows [r0, r0+64) of K - mean, one INT8 scale for the block.
+template <int D>
 __device__ __forceinline__ void quant_k_block(const PrepParams& p, int b, int h, int kb, float* red) {
+    using Sh = PrepShape<D>;
     const int bh = b * p.H + h;
     const int tid = threadIdx.x;
     const int lk = clamp_len(p.kv_len, b, p.Nkv);
-    const int dg = tid & 15, rs = tid >> 4;
+    const int dg = tid % Sh::kGroups, rs = tid / Sh::kGroups;
     const int d0 = dg * 8, r0 = kb * kBKS;
     float mean[8];
     {
-        const float4* mp = reinterpret_cast<const float4*>(p.k_mean + (int64_t)bh * kD + d0);
+        const float4* mp = reinterpret_cast<const float4*>(p.k_mean + (int64_t)bh * D + d0);
         const float4 m0 = mp[0], m1 = mp[1];
         mean[0] = m0.x; mean[1] = m0.y; mean[2] = m0.z; mean[3] = m0.w;
         mean[4] = m1.x; mean[5] = m1.y; mean[6] = m1.z; mean[7] = m1.w;
     }
-    uint4 xr[4];
+    uint4 xr[Sh::kKPasses];
     const uint16_t* kp = p.k + b * p.ksb + h * p.ksh + d0;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int r = r0 + rs + 16 * i;
+    for (int i = 0; i < Sh::kKPasses; ++i) {
+        const int r = r0 + rs + Sh::kRowsPerPass * i;
         xr[i] = (r < lk) ? ldg16(kp + (int64_t)r * p.ksn) : make_uint4(0, 0, 0, 0);
     }
     float amax = 0.f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int r = r0 + rs + 16 * i;
+    for (int i = 0; i < Sh::kKPasses; ++i) {
+        const int r = r0 + rs + Sh::kRowsPerPass * i;
         if (r < lk) {
             float x[8];
             unpack8(xr[i], x);
@@ -272,28 +294,30 @@ __device__ __forceinline__ void quant_k_block(const PrepParams& p, int b, int h,
     const float inv = amax > 0.f ? __fdiv_rn(127.0f, amax) : 0.f;
     if (tid == 0) p.k_scale[(int64_t)bh * p.nk_blocks + kb] = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 0.f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int r = r0 + rs + 16 * i;
+    for (int i = 0; i < Sh::kKPasses; ++i) {
+        const int r = r0 + rs + Sh::kRowsPerPass * i;
         if (r >= p.Nkv) continue;
         float x[8];
         unpack8(xr[i], x);
         int c[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) c[e] = (r < lk) ? int8_code(__fsub_rn(x[e], mean[e]), inv) : 0;
-        store_row_codes(c, p.k16, p.k8, ((int64_t)bh * p.Nkv + r) * kD + d0);
+        store_row_codes(c, p.k16, p.k8, ((int64_t)bh * p.Nkv + r) * D + d0);
     }
 }
 
-// V tile: tokens [t0, t0+64) -> e4m3 per channel, stored [d][token].
+// V tile: tokens [t0, t0 + 8192/D) -> e4m3 per channel, stored [d][token].
+template <int D>
 __device__ __forceinline__ void quant_v_tile(const PrepParams& p, int b, int h, int vt, uint32_t* vtile) {
+    using Sh = PrepShape<D>;
     const int bh = b * p.H + h;
     const int tid = threadIdx.x;
     const int lk = clamp_len(p.kv_len, b, p.Nkv);
-    const int tq = tid & 15, dg = tid >> 4;           // 4 tokens x 8 channels per thread
-    const int d0 = dg * 8, t0 = vt * 64;
+    const int tq = tid % Sh::kTokGroups, dg = tid / Sh::kTokGroups;   // 4 tokens x 8 channels per thread
+    const int d0 = dg * 8, t0 = vt * Sh::kVTokens;
     float inv[8];
     {
-        const float4* ip = reinterpret_cast<const float4*>(p.v_inv + (int64_t)bh * kD + d0);
+        const float4* ip = reinterpret_cast<const float4*>(p.v_inv + (int64_t)bh * D + d0);
         const float4 i0 = ip[0], i1 = ip[1];
         inv[0] = i0.x; inv[1] = i0.y; inv[2] = i0.z; inv[3] = i0.w;
         inv[4] = i1.x; inv[5] = i1.y; inv[6] = i1.z; inv[7] = i1.w;
@@ -322,50 +346,61 @@ __device__ __forceinline__ void quant_v_tile(const PrepParams& p, int b, int h, 
         }
     }
 #pragma unroll
-    for (int e = 0; e < 8; ++e) vtile[(d0 + e) * 20 + tq] = word[e];
+    for (int e = 0; e < 8; ++e) vtile[(d0 + e) * Sh::kVStride + tq] = word[e];
     __syncthreads();
+    constexpr int kParts = Sh::kVTokens / 16;           // 16-token chunks per channel row
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-        const int chunk = tid + 256 * k;                // 128 rows x 4 chunks of 16 tokens
-        const int d = chunk >> 2, part = chunk & 3;
+        const int chunk = tid + 256 * k;                // D rows x kParts chunks = 512
+        const int d = chunk / kParts, part = chunk % kParts;
         const int t = t0 + part * 16;
         if (t < p.nkv_pad) {
-            const uint4 w = *reinterpret_cast<const uint4*>(&vtile[d * 20 + part * 4]);
-            *reinterpret_cast<uint4*>(p.v8t + ((int64_t)bh * kD + d) * p.nkv_pad + t) = w;
+            const uint4 w = *reinterpret_cast<const uint4*>(&vtile[d * Sh::kVStride + part * 4]);
+            *reinterpret_cast<uint4*>(p.v8t + ((int64_t)bh * D + d) * p.nkv_pad + t) = w;
         }
     }
 }
 
+template <int D>
 __global__ void __launch_bounds__(256, 4) prep_kv_kernel(const PrepParams p) {
     __shared__ float red[8];
-    __shared__ __align__(16) uint32_t vtile[kD * 20];   // [d][16 words of 4 tokens + 4 pad]
+    __shared__ __align__(16) uint32_t vtile[D * PrepShape<D>::kVStride];   // [d][words of 4 tokens + 4 pad]
     const int b = blockIdx.z, h = blockIdx.y;
-    if ((int)blockIdx.x < p.nk_blocks) quant_k_block(p, b, h, blockIdx.x, red);
-    else quant_v_tile(p, b, h, blockIdx.x - p.nk_blocks, vtile);
+    if ((int)blockIdx.x < p.nk_blocks) quant_k_block<D>(p, b, h, blockIdx.x, red);
+    else quant_v_tile<D>(p, b, h, blockIdx.x - p.nk_blocks, vtile);
+}
+
+template <int D>
+cudaError_t launch_prep_d(const PrepParams& p, cudaStream_t s, int* launches) {
+    using Sh = PrepShape<D>;
+    *launches = 0;
+    {
+        const int n_stat_blocks = (p.n_chunks + Sh::kStatChunks - 1) / Sh::kStatChunks;
+        dim3 grid((unsigned)(n_stat_blocks + p.nq_blocks), (unsigned)p.H, (unsigned)p.B);
+        prep_stats_q_kernel<D><<<grid, 256, 0, s>>>(p);
+        ++*launches;
+    }
+    {
+        dim3 grid((unsigned)p.H, (unsigned)p.B);
+        prep_finalize_kernel<D><<<grid, D, 0, s>>>(p);
+        ++*launches;
+    }
+    {
+        const int n_vtiles = (p.nkv_pad + Sh::kVTokens - 1) / Sh::kVTokens;
+        dim3 grid((unsigned)(p.nk_blocks + n_vtiles), (unsigned)p.H, (unsigned)p.B);
+        prep_kv_kernel<D><<<grid, 256, 0, s>>>(p);
+        ++*launches;
+    }
+    return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t s, int* launches) {
     *launches = 0;
-    {
-        const int n_stat_blocks = (p.n_chunks + kStatChunksPerBlock - 1) / kStatChunksPerBlock;
-        dim3 grid((unsigned)(n_stat_blocks + p.nq_blocks), (unsigned)p.H, (unsigned)p.B);
-        prep_stats_q_kernel<<<grid, 256, 0, s>>>(p);
-        ++*launches;
-    }
-    {
-        dim3 grid((unsigned)p.H, (unsigned)p.B);
-        prep_finalize_kernel<<<grid, 128, 0, s>>>(p);
-        ++*launches;
-    }
-    {
-        const int n_vtiles = (p.nkv_pad + 63) / 64;
-        dim3 grid((unsigned)(p.nk_blocks + n_vtiles), (unsigned)p.H, (unsigned)p.B);
-        prep_kv_kernel<<<grid, 256, 0, s>>>(p);
-        ++*launches;
-    }
-    return cudaGetLastError();
+    if (p.D == 64) return launch_prep_d<64>(p, s, launches);
+    if (p.D == 128) return launch_prep_d<128>(p, s, launches);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace sage

@@ -56,7 +56,7 @@ class GpuRun:
                       if w.q_len is not None else None)
         self.kv_len = (torch.tensor(w.kv_len, dtype=torch.int32, device="cuda")
                        if w.kv_len is not None else None)
-        self.bufs = S.alloc_prep_buffers(w.B, w.H, w.Nq, w.Nkv, "cuda", int8_codes=int8_codes)
+        self.bufs = S.alloc_prep_buffers(w.B, w.H, w.Nq, w.Nkv, "cuda", int8_codes=int8_codes, D=w.D)
         self.out = None
 
     def prep(self):
@@ -64,7 +64,7 @@ class GpuRun:
         torch.cuda.synchronize()
         return self
 
-    def attn(self, fill=None):
+    def attn(self, fill=None, causal=False):
         w = self.w
         base = torch.empty((w.B, w.Nq, w.H, w.D), dtype=torch.bfloat16, device="cuda")
         if fill is None:
@@ -72,7 +72,7 @@ class GpuRun:
         else:
             base.fill_(fill)
         self.out = base.permute(0, 2, 1, 3)
-        S.sage_attn_fwd(self.bufs, self.out, self.q_len, self.kv_len, Nkv=w.Nkv)
+        S.sage_attn_fwd(self.bufs, self.out, self.q_len, self.kv_len, Nkv=w.Nkv, causal=causal)
         torch.cuda.synchronize()
         assert S.sage_get_device_status() == S.SAGE_OK
         return self

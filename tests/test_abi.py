@@ -50,11 +50,15 @@ def test_buffer_sizes(lib):
     assert s.v8t == 2 * 16 * 128 * 784
     assert s.q_scale == 2 * 16 * 8 * 4 and s.k_scale == 2 * 16 * 13 * 4
     assert s.workspace == 2 * (2 * 16 * 13 * 128 * 4) + 2 * 16 * 128 * 4
+    s64 = S.buffer_sizes(2, 16, 1000, 777, D=64)
+    assert s64.q16 == 2 * 16 * 1000 * 64 * 2 and s64.v8t == 2 * 16 * 64 * 784
+    assert s64.workspace == 2 * (2 * 16 * 13 * 64 * 4) + 2 * 16 * 64 * 4
 
 
 @pytest.mark.parametrize("shape,code", [((0, 1, 1, 1, 128), S.SAGE_ERR_ARG),
                                         ((1, 1, 1, 0, 128), S.SAGE_ERR_ARG),
-                                        ((1, 1, 1, 1, 64), S.SAGE_ERR_UNSUPPORTED)])
+                                        ((1, 1, 1, 1, 96), S.SAGE_ERR_UNSUPPORTED),
+                                        ((1, 1, 1, 1, 256), S.SAGE_ERR_UNSUPPORTED)])
 def test_buffer_sizes_rejects_bad_shapes(lib, shape, code):
     s = S.sage_sizes()
     assert lib.sage_buffer_sizes(*shape, ctypes.byref(s)) == code
