@@ -137,6 +137,28 @@ int sage_attn_fwd_causal(const sage_prep_buffers* in, const sage_tensor* o,
                          const int32_t* q_len, const int32_t* kv_len,
                          float sm_scale, void* stream);
 
+/* One call from BF16 Q/K/V to the BF16 output, with the Q preparation fused
+ * into the attention kernel (the pages run preparation and attention as
+ * separate stages; fusing them skips the round trip of the Q codes through
+ * device memory).
+ *  q, k, v : BF16 [B,H,Nq,D], [B,H,Nkv,D], [B,H,Nkv,D] views (device), as for
+ *            sage_prep_qkv; o : BF16 [B,H,Nq,D] output (device), as for
+ *            sage_attn_fwd.
+ *  causal  : 0 = the sage_attn_fwd contract, 1 = the sage_attn_fwd_causal one.
+ *  buf     : k16, v8t, k_scale, v_scale, k_mean, workspace (and k8 if not
+ *            NULL) are filled as by sage_prep_qkv; q16 and q8 are not used
+ *            and may be NULL.  q_scale receives the Q block scales of every
+ *            query tile that has a valid row and at least one visible key.
+ * Enqueues the K/V preparation (three kernels) and one attention kernel whose
+ * CTAs load their 128-row BF16 Q block, compute its INT8 scale and codes with
+ * the same arithmetic as sage_prep_qkv, and write the codes over the block in
+ * shared memory before the first QK.  The output is bit-identical to
+ * sage_prep_qkv followed by sage_attn_fwd / sage_attn_fwd_causal. */
+int sage_attention(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
+                   const sage_tensor* o, int B, int H, int Nq, int Nkv, int D,
+                   const int32_t* q_len, const int32_t* kv_len, float sm_scale, int causal,
+                   const sage_prep_buffers* buf, void* stream);
+
 /* The "QK" checkpoint: exact integer scores S[b,h,i,j] = sum_d q8*k8 from the
  * same tensor-core path sage_attn_fwd uses, written as int32 to
  * s [B, H, Nq, Nkv] (device, row-major).  Entries with i >= q_len[b] or

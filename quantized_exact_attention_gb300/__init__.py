@@ -29,7 +29,8 @@ D_HEAD = 128
 HEAD_DIMS = (64, 128)       # head dimensions the kernels are built for
 
 # Names the header declares (checked by the CPU tests against the .so exports).
-EXPORTED = ("sage_buffer_sizes", "sage_prep_qkv", "sage_attn_fwd", "sage_attn_fwd_causal", "sage_qk_int32",
+EXPORTED = ("sage_buffer_sizes", "sage_prep_qkv", "sage_attn_fwd", "sage_attn_fwd_causal", "sage_attention",
+            "sage_qk_int32",
             "sage_attention_host", "sage_get_device_status", "sage_status_string",
             "sage_last_launch_count", "sage_debug_inject_fault", "sage_prep_qkv_noalloc",
             "sage_prep_noalloc_capacity")
@@ -82,6 +83,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                   P(sage_prep_buffers), vp]
     lib.sage_attn_fwd.argtypes = [P(sage_prep_buffers), P(sage_tensor), i, i, i, i, i, vp, vp, f, vp]
     lib.sage_attn_fwd_causal.argtypes = lib.sage_attn_fwd.argtypes
+    lib.sage_attention.argtypes = [P(sage_tensor), P(sage_tensor), P(sage_tensor), P(sage_tensor),
+                                   i, i, i, i, i, vp, vp, f, i, P(sage_prep_buffers), vp]
     lib.sage_qk_int32.argtypes = [P(sage_prep_buffers), vp, i, i, i, i, i, vp, vp, vp]
     lib.sage_attention_host.argtypes = [P(sage_copy), i, P(sage_tensor), P(sage_tensor), P(sage_tensor),
                                         P(sage_prep_buffers), P(sage_tensor), P(sage_copy),
@@ -215,6 +218,19 @@ def sage_attn_fwd(bufs: PrepBuffers, o, q_len=None, kv_len=None, sm_scale: float
     _check(rc, "sage_attn_fwd_causal" if causal else "sage_attn_fwd")
 
 
+def sage_attention(q, k, v, o, bufs: PrepBuffers, q_len=None, kv_len=None, sm_scale: float = 0.0,
+                   causal: bool = False, stream=None):
+    """Enqueue K/V preparation plus the attention kernel that quantizes its own
+    Q blocks, on [B,H,N,D] BF16 views q, k, v and output view o."""
+    B, H, Nq, D = q.shape
+    Nkv = k.shape[2]
+    qs, ks, vs, os_, pb = tensor_desc(q), tensor_desc(k), tensor_desc(v), tensor_desc(o), bufs.c_struct()
+    rc = load_library().sage_attention(ctypes.byref(qs), ctypes.byref(ks), ctypes.byref(vs), ctypes.byref(os_),
+                                       B, H, Nq, Nkv, D, _lens(q_len), _lens(kv_len), float(sm_scale),
+                                       1 if causal else 0, ctypes.byref(pb), _stream_ptr(stream))
+    _check(rc, "sage_attention")
+
+
 def sage_qk_int32(bufs: PrepBuffers, s: torch.Tensor, q_len=None, kv_len=None, stream=None):
     """Enqueue the QK checkpoint kernel; s is int32 [B, H, Nq, Nkv] contiguous."""
     B, H, Nq, Nkv = s.shape
@@ -261,13 +277,18 @@ def sage_debug_inject_fault(mode: int):
 
 
 def attention(q, k, v, q_len=None, kv_len=None, sm_scale: float = 0.0, out=None, int8_codes=False,
-              stream=None, causal: bool = False):
-    """Prep + fused attention on [B,H,N,D] BF16 CUDA views; returns (o, bufs)."""
+              stream=None, causal: bool = False, fused: bool = True):
+    """Attention on [B,H,N,D] BF16 CUDA views; returns (o, bufs).  fused=True
+    uses sage_attention (Q quantized inside the attention kernel); False runs
+    sage_prep_qkv then sage_attn_fwd (every code buffer filled)."""
     B, H, Nq, D = q.shape
     Nkv = k.shape[2]
     bufs = alloc_prep_buffers(B, H, Nq, Nkv, q.device, int8_codes=int8_codes, D=D)
     if out is None:
         out = torch.zeros((B, Nq, H, D), dtype=torch.bfloat16, device=q.device).permute(0, 2, 1, 3)
-    sage_prep_qkv(q, k, v, bufs, q_len, kv_len, stream)
-    sage_attn_fwd(bufs, out, q_len, kv_len, sm_scale, stream, Nkv=Nkv, causal=causal)
+    if fused:
+        sage_attention(q, k, v, out, bufs, q_len, kv_len, sm_scale, causal, stream)
+    else:
+        sage_prep_qkv(q, k, v, bufs, q_len, kv_len, stream)
+        sage_attn_fwd(bufs, out, q_len, kv_len, sm_scale, stream, Nkv=Nkv, causal=causal)
     return out, bufs

@@ -57,6 +57,21 @@ bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, void* base, uint64_t x, u
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D tiled map over a BF16 [B][H][N][D] view with arbitrary element strides
+// (channel fastest), box 64 channels x 128 rows, 128-byte swizzle.
+bool encode_bf16_view(CUtensorMap* m, const void* base, uint64_t D, uint64_t N, uint64_t H, uint64_t B,
+                      int64_t sn, int64_t sh, int64_t sb) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {D, N, H, B};
+    cuuint64_t strides[3] = {(cuuint64_t)sn * 2, (cuuint64_t)sh * 2, (cuuint64_t)sb * 2};
+    cuuint32_t box[4] = {64, 128, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int check_shape(int B, int H, int Nq, int Nkv, int D) {
     if (B <= 0 || H <= 0 || Nq <= 0 || Nkv <= 0) return SAGE_ERR_ARG;
     if (B > 65535 || H > 65535 || Nq > (1 << 24) || Nkv > (1 << 24)) return SAGE_ERR_ARG;
@@ -166,7 +181,7 @@ int sage_prep_qkv(const sage_tensor* q, const sage_tensor* k, const sage_tensor*
     p.pamax = ws + part;
     p.v_inv = ws + 2 * part;
     int launches = 0;
-    rc = status_from(launch_prep(p, static_cast<cudaStream_t>(stream), &launches));
+    rc = status_from(launch_prep(p, true, static_cast<cudaStream_t>(stream), &launches));
     if (rc == SAGE_OK) g_last_launches = launches;
     return rc;
 }
@@ -217,7 +232,8 @@ static int attn_common(const sage_prep_buffers* in, const sage_tensor* o, int32_
     p.fault_mode = fault_mode_for_next_launch;
     fault_mode_for_next_launch = 0;
     int launches = 0;
-    rc = status_from(launch_attn(p, tq, tk, tv, capture, causal, static_cast<cudaStream_t>(stream), &launches));
+    rc = status_from(launch_attn(p, tq, tk, tv, capture, causal, false, static_cast<cudaStream_t>(stream),
+                                 &launches));
     if (rc == SAGE_OK) g_last_launches = launches;
     return rc;
 }
@@ -235,6 +251,81 @@ int sage_attn_fwd_causal(const sage_prep_buffers* in, const sage_tensor* o, int 
 int sage_qk_int32(const sage_prep_buffers* in, int32_t* s, int B, int H, int Nq, int Nkv, int D,
                   const int32_t* q_len, const int32_t* kv_len, void* stream) {
     return attn_common(in, nullptr, s, B, H, Nq, Nkv, D, q_len, kv_len, 0.f, stream, true, false);
+}
+
+int sage_attention(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v, const sage_tensor* o,
+                   int B, int H, int Nq, int Nkv, int D, const int32_t* q_len, const int32_t* kv_len,
+                   float sm_scale, int causal, const sage_prep_buffers* buf, void* stream) {
+    int rc = check_shape(B, H, Nq, Nkv, D);
+    if (rc != SAGE_OK) return rc;
+    if ((rc = check_tensor(q)) != SAGE_OK || (rc = check_tensor(k)) != SAGE_OK ||
+        (rc = check_tensor(v)) != SAGE_OK || (rc = check_tensor(o)) != SAGE_OK)
+        return rc;
+    sage_sizes sz;
+    sage_buffer_sizes(B, H, Nq, Nkv, D, &sz);
+    if (buf == nullptr || !buf->k16 || !buf->v8t || !buf->q_scale || !buf->k_scale || !buf->v_scale ||
+        !buf->k_mean || !buf->workspace)
+        return SAGE_ERR_ARG;
+    const void* ptrs[] = {buf->k16, buf->v8t, buf->q_scale, buf->k_scale, buf->v_scale, buf->k_mean,
+                          buf->workspace};
+    for (const void* ptr : ptrs)
+        if (!aligned16(ptr)) return SAGE_ERR_UNSUPPORTED;
+    if (buf->k8 && !aligned16(buf->k8)) return SAGE_ERR_UNSUPPORTED;
+    if (buf->workspace_bytes < sz.workspace) return SAGE_ERR_ARG;
+    int* status = device_status_ptr();
+    if (status == nullptr) return SAGE_ERR_LAUNCH;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    // K/V preparation only
+    PrepParams pp{};
+    pp.k = static_cast<const uint16_t*>(k->ptr);
+    pp.v = static_cast<const uint16_t*>(v->ptr);
+    pp.ksb = k->stride_b; pp.ksh = k->stride_h; pp.ksn = k->stride_n;
+    pp.vsb = v->stride_b; pp.vsh = v->stride_h; pp.vsn = v->stride_n;
+    pp.B = B; pp.H = H; pp.Nq = Nq; pp.Nkv = Nkv; pp.D = D;
+    pp.nkv_pad = (int)sz.nkv_pad;
+    pp.nq_blocks = (int)ceil_div(Nq, kBQS);
+    pp.nk_blocks = (int)ceil_div(Nkv, kBKS);
+    pp.n_chunks = (int)ceil_div(Nkv, kMeanChunk);
+    pp.q_len = q_len; pp.kv_len = kv_len;
+    pp.k16 = buf->k16; pp.v8t = buf->v8t; pp.k8 = buf->k8;
+    pp.k_scale = buf->k_scale; pp.v_scale = buf->v_scale; pp.k_mean = buf->k_mean;
+    float* ws = static_cast<float*>(buf->workspace);
+    const int64_t part = (int64_t)B * H * pp.n_chunks * D;
+    pp.psum = ws;
+    pp.pamax = ws + part;
+    pp.v_inv = ws + 2 * part;
+    int prep_launches = 0;
+    if ((rc = status_from(launch_prep(pp, false, s, &prep_launches))) != SAGE_OK) return rc;
+
+    // attention with the Q quantization in its prologue
+    const uint64_t bh = (uint64_t)B * H, d = (uint64_t)D;
+    CUtensorMap tq, tk, tv;
+    if (!encode_bf16_view(&tq, q->ptr, d, (uint64_t)Nq, (uint64_t)H, (uint64_t)B, q->stride_n, q->stride_h,
+                          q->stride_b) ||
+        !encode_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, buf->k16, d, (uint64_t)Nkv, bh, d * 2,
+                   (uint64_t)Nkv * d * 2, 64, 128) ||
+        !encode_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, buf->v8t, (uint64_t)sz.nkv_pad, d, bh,
+                   (uint64_t)sz.nkv_pad, (uint64_t)sz.nkv_pad * d, 128, (uint32_t)D))
+        return encode_fn() ? SAGE_ERR_UNSUPPORTED : SAGE_ERR_DRIVER;
+    AttnParams p{};
+    p.k_scale = buf->k_scale; p.v_scale = buf->v_scale;
+    p.q_scale_out = buf->q_scale;
+    p.q_len = q_len; p.kv_len = kv_len;
+    p.o = static_cast<uint16_t*>(const_cast<void*>(o->ptr));
+    p.osb = o->stride_b; p.osh = o->stride_h; p.osn = o->stride_n;
+    p.B = B; p.H = H; p.Nq = Nq; p.Nkv = Nkv; p.D = D;
+    p.nq_blocks = pp.nq_blocks;
+    p.nk_blocks = pp.nk_blocks;
+    const double scale = sm_scale > 0.f ? (double)sm_scale : 1.0 / std::sqrt((double)D);
+    p.c = (float)(scale * (1.0 / std::log(2.0)));
+    p.status = status;
+    p.fault_mode = fault_mode_for_next_launch;
+    fault_mode_for_next_launch = 0;
+    int launches = 0;
+    rc = status_from(launch_attn(p, tq, tk, tv, false, causal != 0, true, s, &launches));
+    if (rc == SAGE_OK) g_last_launches = launches + prep_launches;
+    return rc;
 }
 
 int sage_attention_host(const sage_copy* inputs, int n_inputs, const sage_tensor* q, const sage_tensor* k,

@@ -42,6 +42,7 @@
 
 #include "sage_internal.h"
 #include "sage_ptx.cuh"
+#include "sage_quant.cuh"
 
 namespace sage {
 namespace {
@@ -70,7 +71,8 @@ enum Bar : uint32_t {
     B_XM = B_AFREE + 2,         // [buf][quarter]: the two halves of 32 rows exchanged maxima
     B_LFULL = B_XM + 8,
     B_DRAIN = B_LFULL + 1,
-    B_COUNT = B_DRAIN + 1
+    B_QREADY = B_DRAIN + 1,     // fused Q: codes written over the BF16 tile
+    B_COUNT = B_QREADY + 1
 };
 
 // Shared-memory map for head dimension D (offsets from a 1024-byte aligned
@@ -92,7 +94,8 @@ struct Smem {
     static constexpr uint32_t OFF_VS = OFF_L + 2 * 128 * 4;                           // float [D]
     static constexpr uint32_t OFF_TMEM = OFF_VS + 128 * 4;                            // u32
     static constexpr uint32_t OFF_ABORT = OFF_TMEM + 16;                              // int
-    static constexpr uint32_t kSmemUsed = OFF_ABORT + 16;
+    static constexpr uint32_t OFF_RED = OFF_ABORT + 16;                               // float [16]
+    static constexpr uint32_t kSmemUsed = OFF_RED + 64;
     static constexpr uint32_t kSmemBytes = kSmemUsed + 1024;                          // + alignment slack
 };
 
@@ -137,7 +140,10 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
 // kCausal: key j is visible to query i iff j <= i + (Lk - Lq); a CTA visits
 // only the KV tiles up to the diagonal of its last row, and rows that see no
 // key are written as zero.
-template <int D, bool kCapture, bool kCausal>
+// kFusedQ: tm_q maps the caller's BF16 Q (4-D: channel, row, head, batch) and
+// the CTA quantizes its own 128-row Q block (one INT8 scale block) in place in
+// shared memory before the first QK; its scale goes to p.q_scale_out.
+template <int D, bool kCapture, bool kCausal, bool kFusedQ>
 __global__ void __launch_bounds__(kThreads, 1)
 sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
@@ -145,7 +151,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     constexpr uint32_t kTileQBytes = L::kTileQBytes, kTileKBytes = L::kTileKBytes, kTileVBytes = L::kTileVBytes;
     constexpr uint32_t OFF_Q = L::OFF_Q, OFF_K = L::OFF_K, OFF_V = L::OFF_V, OFF_BAR = L::OFF_BAR;
     constexpr uint32_t OFF_ALPHA = L::OFF_ALPHA, OFF_XM = L::OFF_XM, OFF_L = L::OFF_L, OFF_VS = L::OFF_VS;
-    constexpr uint32_t OFF_TMEM = L::OFF_TMEM, OFF_ABORT = L::OFF_ABORT;
+    constexpr uint32_t OFF_TMEM = L::OFF_TMEM, OFF_ABORT = L::OFF_ABORT, OFF_RED = L::OFF_RED;
     constexpr int kDH = D / 2;                              // output channels per correction thread
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_u32(smem_raw);
@@ -205,6 +211,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
         mbar_init(bar(B_LFULL), 256);             // every softmax thread
         mbar_init(bar(B_DRAIN), 1);
+        mbar_init(bar(B_QREADY), 512);            // every softmax and correction thread (fused Q)
         fence_mbar_init();
     }
     if (warp == kWarpMma) {
@@ -221,20 +228,69 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    float fused_qs = 0.f;                                   // fused Q: this block's INT8 scale
+    if constexpr (kFusedQ) {
+        if (warp < 16) {
+            // The softmax and correction warps quantize the CTA's Q block in
+            // place: the BF16 tile and the FP16 code tile have the same element
+            // size and the same 128-byte swizzle, so each 16-byte chunk keeps
+            // its address; the swizzle permutes chunks within a row, so a
+            // chunk's row is its byte offset / 128 within its 64-channel block.
+            const int ct = threadIdx.x;                     // 0..511
+            constexpr int kChunks = (int)(kTileQBytes / 16 / 512);
+            const bool got = warp_wait(bar(B_QFULL), 0, abort_flag);
+            if (!got && lane == 0) record_failure(p, abort_flag, R_SOFTMAX, -1);
+            uint4 xq[kChunks];
+            float amax = 0.f;
+#pragma unroll
+            for (int i = 0; i < kChunks; ++i) {
+                const uint32_t off = (uint32_t)(ct + 512 * i) * 16u;
+                const int r = (int)((off % kHalfBytes) / 128u);
+                xq[i] = got ? *reinterpret_cast<const uint4*>(sgen + OFF_Q + off) : make_uint4(0, 0, 0, 0);
+                if (q0 + r < lq) amax = absmax8(xq[i], amax);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            float* red = reinterpret_cast<float*>(sgen + OFF_RED);
+            if (lane == 0) red[warp] = amax;
+            named_bar_sync(6, 512);                         // every softmax/correction thread, unconditionally
+            amax = red[0];
+#pragma unroll
+            for (int i = 1; i < 16; ++i) amax = fmaxf(amax, red[i]);
+            const float inv = int8_inv(amax);
+            fused_qs = int8_scale(amax);
+            if (ct == 0) p.q_scale_out[(int64_t)bh * p.nq_blocks + qtile] = fused_qs;
+#pragma unroll
+            for (int i = 0; i < kChunks; ++i) {
+                const uint32_t off = (uint32_t)(ct + 512 * i) * 16u;
+                const int r = (int)((off % kHalfBytes) / 128u);
+                float x[8];
+                unpack8(xq[i], x);
+                int c[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) c[e] = (q0 + r < lq) ? int8_code(x[e], inv) : 0;
+                *reinterpret_cast<uint4*>(sgen + OFF_Q + off) = pack_half_codes(c);
+            }
+            fence_proxy_async_smem();                       // codes visible to the tensor core
+            mbar_arrive(bar(B_QREADY));
+        }
+    }
+
     if (warp < 8) {
         // ===================================================== softmax
         const int quarter = warp & 3, half = warp >> 2;
         const int row = quarter * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         float* xm = reinterpret_cast<float*>(sgen + OFF_XM);    // [buf][half][row]
-        const float qs = p.q_scale[(int64_t)bh * p.nq_blocks + qtile];
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
+        const float qs = kFusedQ ? fused_qs : p.q_scale[(int64_t)bh * p.nq_blocks + qtile];
         // this half's 64-key scale block of tile t is 2t + half; load one tile ahead
         const float* kscale = p.k_scale + (int64_t)bh * p.nk_blocks;
         float ks_next = (half * 64 < lk) ? kscale[half] : 0.f;
         int s3 = 0, s3ph = 0;                               // S/P buffer of tile t and its phase
-        for (int t = 0; t < T; ++t, s3 = (s3 == kNS - 1) ? 0 : s3 + 1, s3ph ^= (s3 == 0) ? 1 : 0) {
+        const int T_sm = ok ? T : 0;
+        for (int t = 0; t < T_sm; ++t, s3 = (s3 == kNS - 1) ? 0 : s3 + 1, s3ph ^= (s3 == 0) ? 1 : 0) {
             const int sb = t & 1;
             const float ks = ks_next;
             const int kb_next = 2 * (t + 1) + half;
@@ -440,7 +496,12 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             bool ok = true;
             mbar_arrive_expect_tx(bar(B_QFULL), kTileQBytes);
 #pragma unroll
-            for (int hh = 0; hh < D / 64; ++hh) tma_load_3d(sQ + hh * kHalfBytes, &tm_q, hh * 64, q0, bh, bar(B_QFULL));
+            for (int hh = 0; hh < D / 64; ++hh) {
+                if constexpr (kFusedQ)
+                    tma_load_4d(sQ + hh * kHalfBytes, &tm_q, hh * 64, q0, h, b, bar(B_QFULL));
+                else
+                    tma_load_3d(sQ + hh * kHalfBytes, &tm_q, hh * 64, q0, bh, bar(B_QFULL));
+            }
             auto load_k = [&](int t) -> bool {
                 const int st = t % kNK;
                 if (t >= kNK && !mbar_wait(bar(B_KEMPTY + st), ((t / kNK) - 1) & 1, abort_flag)) return false;
@@ -487,7 +548,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             constexpr uint32_t kIdescQK = idesc_f32acc(0u, 128u, 128u);   // F16 x F16 -> F32
             constexpr uint32_t kIdescPV = idesc_f16acc(0u, 128u, (uint32_t)D);   // E4M3 x E4M3 -> F16
             const uint32_t sQ = sbase + OFF_Q;
-            bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag);
+            bool ok = mbar_wait(bar(kFusedQ ? B_QREADY : B_QFULL), 0, abort_flag);
             int fail_tile = 0;
             // Shared-memory descriptors are built once.  Their start-address field
             // holds (address >> 4) in the low 14 bits; every operand lies below
@@ -560,7 +621,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
 }
 
-template <int D, bool kCapture, bool kCausal>
+template <int D, bool kCapture, bool kCausal, bool kFusedQ = false>
 cudaError_t launch_one(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, cudaStream_t s) {
     static bool attr_set[64] = {};                          // per device, per instantiation
@@ -569,30 +630,34 @@ cudaError_t launch_one(const AttnParams& p, const CUtensorMap& tq, const CUtenso
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(sage_attn_kernel<D, kCapture, kCausal>,
+        cudaError_t e = cudaFuncSetAttribute(sage_attn_kernel<D, kCapture, kCausal, kFusedQ>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
     dim3 grid((unsigned)((p.Nq + 127) / 128), (unsigned)p.H, (unsigned)p.B);
-    sage_attn_kernel<D, kCapture, kCausal><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+    sage_attn_kernel<D, kCapture, kCausal, kFusedQ><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_d(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                     bool capture, bool causal, cudaStream_t s) {
+                     bool capture, bool causal, bool fused_q, cudaStream_t s) {
     if (capture) return launch_one<D, true, false>(p, tq, tk, tv, s);
+    if (fused_q)
+        return causal ? launch_one<D, false, true, true>(p, tq, tk, tv, s)
+                      : launch_one<D, false, false, true>(p, tq, tk, tv, s);
     return causal ? launch_one<D, false, true>(p, tq, tk, tv, s) : launch_one<D, false, false>(p, tq, tk, tv, s);
 }
 
 }  // namespace
 
 cudaError_t launch_attn(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                        const CUtensorMap& tv, bool capture, bool causal, cudaStream_t s, int* launches) {
+                        const CUtensorMap& tv, bool capture, bool causal, bool fused_q, cudaStream_t s,
+                        int* launches) {
     *launches = 1;
-    if (p.D == 128) return launch_d<128>(p, tq, tk, tv, capture, causal, s);
-    if (p.D == 64) return launch_d<64>(p, tq, tk, tv, capture, causal, s);
+    if (p.D == 128) return launch_d<128>(p, tq, tk, tv, capture, causal, fused_q, s);
+    if (p.D == 64) return launch_d<64>(p, tq, tk, tv, capture, causal, fused_q, s);
     return cudaErrorInvalidValue;
 }
 

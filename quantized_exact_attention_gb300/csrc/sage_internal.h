@@ -57,6 +57,7 @@ struct AttnParams {
     float c;                               // fp32(sm_scale * log2(e))
     int* status;                           // device status words
     int fault_mode;                        // test hook: 0 = none
+    float* q_scale_out;                    // fused Q only: per-block Q scales written by the kernel
 };
 
 // Device status word layout: [0] first error code, [1] block id, [2] role, [3] tile.
@@ -64,8 +65,12 @@ constexpr int kStatusWords = 4;
 
 int* device_status_ptr();                  // per-device address of the status words
 
-cudaError_t launch_prep(const PrepParams& p, cudaStream_t s, int* launches);
+// with_q = false: K/V statistics and quantization only (Q is quantized by the
+// attention kernel of the fused entry point).
+cudaError_t launch_prep(const PrepParams& p, bool with_q, cudaStream_t s, int* launches);
+// fused_q: tq maps BF16 Q and each CTA quantizes its own Q block.
 cudaError_t launch_attn(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                        const CUtensorMap& tv, bool capture, bool causal, cudaStream_t s, int* launches);
+                        const CUtensorMap& tv, bool capture, bool causal, bool fused_q, cudaStream_t s,
+                        int* launches);
 
 }  // namespace sage

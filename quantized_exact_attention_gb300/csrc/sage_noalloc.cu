@@ -106,6 +106,6 @@ extern "C" int sage_prep_qkv_noalloc(const sage_tensor* q, const sage_tensor* k,
     p.pamax = scratch + part;
     p.v_inv = scratch + 2 * part;
     int launches = 0;
-    return launch_prep(p, static_cast<cudaStream_t>(stream), &launches) == cudaSuccess ? SAGE_OK
+    return launch_prep(p, true, static_cast<cudaStream_t>(stream), &launches) == cudaSuccess ? SAGE_OK
                                                                                          : SAGE_ERR_LAUNCH;
 }

@@ -19,6 +19,7 @@
 #include <cuda_fp8.h>
 
 #include "sage_internal.h"
+#include "sage_quant.cuh"
 
 namespace sage {
 namespace {
@@ -43,27 +44,6 @@ __device__ __forceinline__ int clamp_len(const int32_t* lens, int b, int n) {
     return v < 0 ? 0 : (v > n ? n : v);
 }
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-__device__ __forceinline__ void unpack8(const uint4& u, float (&x)[8]) {
-    x[0] = bf16_lo(u.x); x[1] = bf16_hi(u.x);
-    x[2] = bf16_lo(u.y); x[3] = bf16_hi(u.y);
-    x[4] = bf16_lo(u.z); x[5] = bf16_hi(u.z);
-    x[6] = bf16_lo(u.w); x[7] = bf16_hi(u.w);
-}
-
-// |x| of 8 packed BF16 values, maximum folded into m (the sign bit is cleared
-// on the packed words: BF16 -> FP32 widening is exact, so this equals the
-// maximum of |x| over the widened values)
-__device__ __forceinline__ float absmax8(const uint4& u, float m) {
-    float x[8];
-    unpack8(make_uint4(u.x & 0x7FFF7FFFu, u.y & 0x7FFF7FFFu, u.z & 0x7FFF7FFFu, u.w & 0x7FFF7FFFu), x);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) m = fmaxf(m, x[e]);
-    return m;
-}
-
 __device__ __forceinline__ uint4 ldg16(const uint16_t* p) {
     return __ldg(reinterpret_cast<const uint4*>(p));
 }
@@ -80,24 +60,10 @@ __device__ __forceinline__ float block_max_256(float v, float* red) {
     return r;
 }
 
-__device__ __forceinline__ uint32_t half_code(int c) {
-    return (uint32_t)__half_as_ushort(__int2half_rn(c));
-}
-
-__device__ __forceinline__ int int8_code(float x, float inv) {
-    int c = __float2int_rn(__fmul_rn(x, inv));
-    return c > 127 ? 127 : (c < -127 ? -127 : c);
-}
-
 // Store the INT8 codes of one row's 8 channels as FP16 images (and as INT8
 // bytes when requested).
 __device__ __forceinline__ void store_row_codes(const int (&c)[8], uint16_t* img, int8_t* bytes, int64_t off) {
-    uint4 hv;
-    hv.x = half_code(c[0]) | (half_code(c[1]) << 16);
-    hv.y = half_code(c[2]) | (half_code(c[3]) << 16);
-    hv.z = half_code(c[4]) | (half_code(c[5]) << 16);
-    hv.w = half_code(c[6]) | (half_code(c[7]) << 16);
-    *reinterpret_cast<uint4*>(img + off) = hv;
+    *reinterpret_cast<uint4*>(img + off) = pack_half_codes(c);
     if (bytes != nullptr) {
         uint2 bv;
         bv.x = (uint32_t)(c[0] & 0xFF) | ((uint32_t)(c[1] & 0xFF) << 8) |
@@ -185,8 +151,8 @@ __device__ __forceinline__ void quant_q_block(const PrepParams& p, int b, int h,
 #pragma unroll
     for (int i = 0; i < Sh::kQPasses; ++i) amax = absmax8(xr[i], amax);
     amax = block_max_256(amax, red);
-    const float inv = amax > 0.f ? __fdiv_rn(127.0f, amax) : 0.f;
-    if (tid == 0) p.q_scale[(int64_t)bh * p.nq_blocks + qb] = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 0.f;
+    const float inv = int8_inv(amax);
+    if (tid == 0) p.q_scale[(int64_t)bh * p.nq_blocks + qb] = int8_scale(amax);
 #pragma unroll
     for (int i = 0; i < Sh::kQPasses; ++i) {
         const int r = r0 + rs + Sh::kRowsPerPass * i;
@@ -291,8 +257,8 @@ __device__ __forceinline__ void quant_k_block(const PrepParams& p, int b, int h,
         }
     }
     amax = block_max_256(amax, red);
-    const float inv = amax > 0.f ? __fdiv_rn(127.0f, amax) : 0.f;
-    if (tid == 0) p.k_scale[(int64_t)bh * p.nk_blocks + kb] = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 0.f;
+    const float inv = int8_inv(amax);
+    if (tid == 0) p.k_scale[(int64_t)bh * p.nk_blocks + kb] = int8_scale(amax);
 #pragma unroll
     for (int i = 0; i < Sh::kKPasses; ++i) {
         const int r = r0 + rs + Sh::kRowsPerPass * i;
@@ -371,12 +337,14 @@ __global__ void __launch_bounds__(256, 4) prep_kv_kernel(const PrepParams p) {
 }
 
 template <int D>
-cudaError_t launch_prep_d(const PrepParams& p, cudaStream_t s, int* launches) {
+cudaError_t launch_prep_d(const PrepParams& p, bool with_q, cudaStream_t s, int* launches) {
     using Sh = PrepShape<D>;
     *launches = 0;
     {
+        // Q blocks follow the statistics blocks in the grid; without Q they are
+        // simply not launched
         const int n_stat_blocks = (p.n_chunks + Sh::kStatChunks - 1) / Sh::kStatChunks;
-        dim3 grid((unsigned)(n_stat_blocks + p.nq_blocks), (unsigned)p.H, (unsigned)p.B);
+        dim3 grid((unsigned)(n_stat_blocks + (with_q ? p.nq_blocks : 0)), (unsigned)p.H, (unsigned)p.B);
         prep_stats_q_kernel<D><<<grid, 256, 0, s>>>(p);
         ++*launches;
     }
@@ -396,10 +364,10 @@ cudaError_t launch_prep_d(const PrepParams& p, cudaStream_t s, int* launches) {
 
 }  // namespace
 
-cudaError_t launch_prep(const PrepParams& p, cudaStream_t s, int* launches) {
+cudaError_t launch_prep(const PrepParams& p, bool with_q, cudaStream_t s, int* launches) {
     *launches = 0;
-    if (p.D == 64) return launch_prep_d<64>(p, s, launches);
-    if (p.D == 128) return launch_prep_d<128>(p, s, launches);
+    if (p.D == 64) return launch_prep_d<64>(p, with_q, s, launches);
+    if (p.D == 128) return launch_prep_d<128>(p, with_q, s, launches);
     return cudaErrorInvalidValue;
 }
 

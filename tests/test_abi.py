@@ -107,6 +107,29 @@ def test_attn_rejects_bad_arguments_before_touching_the_gpu(lib):
                                    None) == S.SAGE_ERR_ARG
 
 
+def test_fused_entry_and_causal_reject_bad_arguments_before_touching_the_gpu(lib):
+    t, o = _fake_tensor(), _fake_tensor()
+    b = _fake_bufs(q16=None)                                   # q16/q8 are not used by the fused entry
+
+    def call(q=t, k=t, v=t, out=o, bufs=b, shape=(1, 4, 256, 256, 128), causal=0):
+        return lib.sage_attention(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), ctypes.byref(out), *shape,
+                                  None, None, 0.0, causal, ctypes.byref(bufs), None)
+
+    assert call(q=_fake_tensor(ptr=0)) == S.SAGE_ERR_ARG
+    assert call(out=_fake_tensor(ptr=0x10004)) == S.SAGE_ERR_UNSUPPORTED
+    assert call(v=_fake_tensor(sh=12)) == S.SAGE_ERR_UNSUPPORTED
+    assert call(bufs=_fake_bufs(k16=None)) == S.SAGE_ERR_ARG
+    assert call(bufs=_fake_bufs(workspace_bytes=16)) == S.SAGE_ERR_ARG
+    assert call(bufs=_fake_bufs(v8t=0x40008)) == S.SAGE_ERR_UNSUPPORTED
+    assert call(shape=(1, 4, 256, 256, 96)) == S.SAGE_ERR_UNSUPPORTED
+    assert call(shape=(1, 4, 0, 256, 128), causal=1) == S.SAGE_ERR_ARG
+    assert lib.sage_attention(None, None, None, None, 1, 1, 1, 1, 128, None, None, 0.0, 0, None,
+                              None) == S.SAGE_ERR_ARG
+    o_bad = _fake_tensor(ptr=0x10004)
+    assert lib.sage_attn_fwd_causal(ctypes.byref(_fake_bufs()), ctypes.byref(o_bad), 1, 1, 128, 128, 64, None,
+                                    None, 0.0, None) == S.SAGE_ERR_UNSUPPORTED
+
+
 def test_status_strings(lib):
     for code in (0, -1, -2, -3, -4, -5):
         assert S.status_string(code) not in ("", "unknown status")
