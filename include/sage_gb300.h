@@ -167,6 +167,37 @@ int sage_qk_int32(const sage_prep_buffers* in, int32_t* s,
                   int B, int H, int Nq, int Nkv, int D,
                   const int32_t* q_len, const int32_t* kv_len, void* stream);
 
+/* Stage checkpoints of one query tile (device buffers, caller-owned).  T is
+ * the number of 128-key tiles the tile visits: ceil(kv_len/128), or up to its
+ * diagonal for the causal form; size every buffer for T = ceil(Nkv/128).
+ * Scale conventions: m, alpha, p8, pv16 and ro are the contract's values (m in
+ * the log2 domain of the scaled scores); l and recip carry the 448 scale of P,
+ * i.e. l = 448 * sum(p) and recip = 1 / (448 * sum(p)). */
+typedef struct {
+    float* m;          /* [T][128]       running maximum after tile t */
+    float* l;          /* [T][2][128]    running sum of each half row (keys 0-63, 64-127 of every
+                                         tile) after tile t; the row's l is their sum */
+    float* alpha;      /* [T][128]       rescale factor 2^(m_old - m_new) of tile t */
+    uint8_t* p8;       /* [T][128][128]  e4m3 P bytes of tile t, key index fastest */
+    uint16_t* pv16;    /* [T][128][D]    FP16 PV tile sums (bit patterns) */
+    float* ro;         /* [T][128][D]    FP32 running output after tile t */
+    float* recip;      /* [128]          reciprocal of the final l */
+} sage_checkpoints;
+
+/* The checkpoint list of Experiment Log, "Phase 2B Fixed Aligned Numerical
+ * Prototype" (QK, m, d, FP8 probability, rescale, FP16 PV, FP32 RO,
+ * reciprocal) for one query tile: runs the attention kernel of sage_attn_fwd
+ * (causal = 0) or sage_attn_fwd_causal (causal = 1) as a single CTA for query
+ * rows [128*qtile, 128*qtile + 128) of head (b, h), writing that tile's output
+ * rows to o as usual and its stage values to ck (rows >= q_len hold
+ * don't-care values).  The QK checkpoint is sage_qk_int32.  Arguments as for
+ * sage_attn_fwd; SAGE_ERR_ARG for a NULL checkpoint buffer or an out-of-range
+ * (b, h, qtile), SAGE_ERR_UNSUPPORTED for a buffer not 16-byte aligned. */
+int sage_attn_checkpoints(const sage_prep_buffers* in, const sage_tensor* o,
+                          int B, int H, int Nq, int Nkv, int D,
+                          const int32_t* q_len, const int32_t* kv_len, float sm_scale, int causal,
+                          int b, int h, int qtile, const sage_checkpoints* ck, void* stream);
+
 /* One host<->device region copied with one cudaMemcpyAsync. */
 typedef struct {
     const void* host;

@@ -30,7 +30,7 @@ HEAD_DIMS = (64, 128)       # head dimensions the kernels are built for
 
 # Names the header declares (checked by the CPU tests against the .so exports).
 EXPORTED = ("sage_buffer_sizes", "sage_prep_qkv", "sage_attn_fwd", "sage_attn_fwd_causal", "sage_attention",
-            "sage_qk_int32",
+            "sage_attn_checkpoints", "sage_qk_int32",
             "sage_attention_host", "sage_get_device_status", "sage_status_string",
             "sage_last_launch_count", "sage_debug_inject_fault", "sage_prep_qkv_noalloc",
             "sage_prep_noalloc_capacity")
@@ -61,6 +61,10 @@ class sage_sizes(ctypes.Structure):
                  "workspace")] + [("nkv_pad", ctypes.c_int64)]
 
 
+class sage_checkpoints(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("m", "l", "alpha", "p8", "pv16", "ro", "recip")]
+
+
 class sage_copy(ctypes.Structure):
     _fields_ = [("host", ctypes.c_void_p), ("device", ctypes.c_void_p), ("bytes", ctypes.c_size_t)]
 
@@ -83,6 +87,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                   P(sage_prep_buffers), vp]
     lib.sage_attn_fwd.argtypes = [P(sage_prep_buffers), P(sage_tensor), i, i, i, i, i, vp, vp, f, vp]
     lib.sage_attn_fwd_causal.argtypes = lib.sage_attn_fwd.argtypes
+    lib.sage_attn_checkpoints.argtypes = [P(sage_prep_buffers), P(sage_tensor), i, i, i, i, i, vp, vp, f, i,
+                                          i, i, i, P(sage_checkpoints), vp]
     lib.sage_attention.argtypes = [P(sage_tensor), P(sage_tensor), P(sage_tensor), P(sage_tensor),
                                    i, i, i, i, i, vp, vp, f, i, P(sage_prep_buffers), vp]
     lib.sage_qk_int32.argtypes = [P(sage_prep_buffers), vp, i, i, i, i, i, vp, vp, vp]
@@ -229,6 +235,27 @@ def sage_attention(q, k, v, o, bufs: PrepBuffers, q_len=None, kv_len=None, sm_sc
                                        B, H, Nq, Nkv, D, _lens(q_len), _lens(kv_len), float(sm_scale),
                                        1 if causal else 0, ctypes.byref(pb), _stream_ptr(stream))
     _check(rc, "sage_attention")
+
+
+def sage_attn_checkpoints(bufs: PrepBuffers, o, b: int, h: int, qtile: int, q_len=None, kv_len=None,
+                          sm_scale: float = 0.0, causal: bool = False, stream=None, Nkv: int | None = None):
+    """Run one query tile as a single CTA and return its stage checkpoints
+    (dict of device tensors: m, l, alpha, p8, pv16, ro, recip; see the header)."""
+    B, H, Nq, D = o.shape
+    Nkv = bufs.k16.shape[2] if Nkv is None else Nkv
+    T = (Nkv + 127) // 128
+    dev = o.device
+    z = lambda shape, dt: torch.zeros(shape, dtype=dt, device=dev)  # noqa: E731
+    ck = dict(m=z((T, 128), torch.float32), l=z((T, 2, 128), torch.float32), alpha=z((T, 128), torch.float32),
+              p8=z((T, 128, 128), torch.uint8), pv16=z((T, 128, D), torch.float16),
+              ro=z((T, 128, D), torch.float32), recip=z((128,), torch.float32))
+    cs = sage_checkpoints(*[ck[n].data_ptr() for n in ("m", "l", "alpha", "p8", "pv16", "ro", "recip")])
+    os_, pb = tensor_desc(o), bufs.c_struct()
+    rc = load_library().sage_attn_checkpoints(ctypes.byref(pb), ctypes.byref(os_), B, H, Nq, Nkv, D,
+                                              _lens(q_len), _lens(kv_len), float(sm_scale), 1 if causal else 0,
+                                              b, h, qtile, ctypes.byref(cs), _stream_ptr(stream))
+    _check(rc, "sage_attn_checkpoints")
+    return ck
 
 
 def sage_qk_int32(bufs: PrepBuffers, s: torch.Tensor, q_len=None, kv_len=None, stream=None):

@@ -188,7 +188,7 @@ int sage_prep_qkv(const sage_tensor* q, const sage_tensor* k, const sage_tensor*
 
 static int attn_common(const sage_prep_buffers* in, const sage_tensor* o, int32_t* s_out, int B, int H, int Nq,
                        int Nkv, int D, const int32_t* q_len, const int32_t* kv_len, float sm_scale,
-                       void* stream, bool capture, bool causal) {
+                       void* stream, bool capture, bool causal, const CkptParams* ck = nullptr) {
     int rc = check_shape(B, H, Nq, Nkv, D);
     if (rc != SAGE_OK) return rc;
     sage_sizes sz;
@@ -232,8 +232,14 @@ static int attn_common(const sage_prep_buffers* in, const sage_tensor* o, int32_
     p.fault_mode = fault_mode_for_next_launch;
     fault_mode_for_next_launch = 0;
     int launches = 0;
-    rc = status_from(launch_attn(p, tq, tk, tv, capture, causal, false, static_cast<cudaStream_t>(stream),
-                                 &launches));
+    if (ck != nullptr) {
+        p.ck = *ck;
+        rc = status_from(launch_attn_checkpoints(p, tq, tk, tv, causal, static_cast<cudaStream_t>(stream)));
+        launches = 1;
+    } else {
+        rc = status_from(launch_attn(p, tq, tk, tv, capture, causal, false, static_cast<cudaStream_t>(stream),
+                                     &launches));
+    }
     if (rc == SAGE_OK) g_last_launches = launches;
     return rc;
 }
@@ -246,6 +252,22 @@ int sage_attn_fwd(const sage_prep_buffers* in, const sage_tensor* o, int B, int 
 int sage_attn_fwd_causal(const sage_prep_buffers* in, const sage_tensor* o, int B, int H, int Nq, int Nkv, int D,
                          const int32_t* q_len, const int32_t* kv_len, float sm_scale, void* stream) {
     return attn_common(in, o, nullptr, B, H, Nq, Nkv, D, q_len, kv_len, sm_scale, stream, false, true);
+}
+
+int sage_attn_checkpoints(const sage_prep_buffers* in, const sage_tensor* o, int B, int H, int Nq, int Nkv, int D,
+                          const int32_t* q_len, const int32_t* kv_len, float sm_scale, int causal, int b, int h,
+                          int qtile, const sage_checkpoints* ck, void* stream) {
+    if (ck == nullptr || !ck->m || !ck->l || !ck->alpha || !ck->p8 || !ck->pv16 || !ck->ro || !ck->recip)
+        return SAGE_ERR_ARG;
+    const void* ptrs[] = {ck->m, ck->l, ck->alpha, ck->p8, ck->pv16, ck->ro, ck->recip};
+    for (const void* ptr : ptrs)
+        if (!aligned16(ptr)) return SAGE_ERR_UNSUPPORTED;
+    if (b < 0 || b >= B || h < 0 || h >= H || qtile < 0 || (int64_t)qtile * 128 >= Nq) return SAGE_ERR_ARG;
+    CkptParams c{};
+    c.m = ck->m; c.l = ck->l; c.alpha = ck->alpha; c.p8 = ck->p8; c.pv16 = ck->pv16; c.ro = ck->ro;
+    c.recip = ck->recip;
+    c.b = b; c.h = h; c.qtile = qtile;
+    return attn_common(in, o, nullptr, B, H, Nq, Nkv, D, q_len, kv_len, sm_scale, stream, false, causal != 0, &c);
 }
 
 int sage_qk_int32(const sage_prep_buffers* in, int32_t* s, int B, int H, int Nq, int Nkv, int D,

@@ -143,7 +143,10 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
 // kFusedQ: tm_q maps the caller's BF16 Q (4-D: channel, row, head, batch) and
 // the CTA quantizes its own 128-row Q block (one INT8 scale block) in place in
 // shared memory before the first QK; its scale goes to p.q_scale_out.
-template <int D, bool kCapture, bool kCausal, bool kFusedQ>
+// kCkpt: a single CTA (p.ck.b, p.ck.h, p.ck.qtile) also writes its per-tile
+// stage values (running max, rescale, running sums, P bytes, FP16 PV sums,
+// FP32 running output, reciprocal) to p.ck.
+template <int D, bool kCapture, bool kCausal, bool kFusedQ, bool kCkpt = false>
 __global__ void __launch_bounds__(kThreads, 1)
 sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
@@ -161,8 +164,8 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     // causal: the longest query tiles start first
-    const int qtile = kCausal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
-    const int h = blockIdx.y, b = blockIdx.z;
+    const int qtile = kCkpt ? p.ck.qtile : (kCausal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x);
+    const int h = kCkpt ? p.ck.h : (int)blockIdx.y, b = kCkpt ? p.ck.b : (int)blockIdx.z;
     const int bh = b * p.H + h;
     const int q0 = qtile * 128;
     const int lq = clamp_len(p.q_len, b, p.Nq);
@@ -393,6 +396,15 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const float tile_sum = (sa0 + sa1) + (sb0 + sb1);
 
             tmem_st16(tmem + lane_base + TM_S + s3 * 128 + half * 16, pk);
+            if constexpr (kCkpt) {
+                uint4* dp = reinterpret_cast<uint4*>(p.ck.p8 + ((int64_t)t * 128 + row) * 128 + half * 64);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) dp[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                if (half == 0) {
+                    p.ck.m[t * 128 + row] = m_new;
+                    p.ck.alpha[t * 128 + row] = alpha;
+                }
+            }
             tmem_wait_st();
             if (half == 0) {
                 if (t >= 2 && !warp_wait(bar(B_AFREE + sb), ((t >> 1) - 1) & 1, abort_flag)) {
@@ -407,6 +419,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             if (half == 0) mbar_arrive(bar(B_AFULL + sb));
             l_run = fmaf(l_run, alpha, tile_sum);
             m_run = (kCausal && l_run == 0.f) ? -INFINITY : m_new;
+            if constexpr (kCkpt) p.ck.l[(t * 2 + half) * 128 + row] = l_run;
         }
         if (!kCapture && ok) {
             l_s[half * 128 + row] = l_run;
@@ -449,6 +462,12 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         tc_fence_before();
                         mbar_arrive(bar(B_PVFREE));
                     }
+                    if constexpr (kCkpt) {
+                        uint4* dp = reinterpret_cast<uint4*>(p.ck.pv16 + ((int64_t)t * 128 + row) * D + half * kDH +
+                                                             c * 32);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) dp[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                    }
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         // RO = RN(RN(RO * alpha) + PV16)
@@ -458,12 +477,18 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         add_f16x2_to(r0, r1, v[i]);
                     }
                 }
+                if constexpr (kCkpt) {
+                    float4* dp = reinterpret_cast<float4*>(p.ck.ro + ((int64_t)t * 128 + row) * D + half * kDH);
+#pragma unroll
+                    for (int i = 0; i < kDH / 4; ++i) dp[i] = make_float4(ro[4 * i], ro[4 * i + 1], ro[4 * i + 2], ro[4 * i + 3]);
+                }
             }
             if (ok && warp_wait(bar(B_LFULL), 0, abort_flag)) {
                 // l carries the 448 scale of P, so (RO / l) * v_scale is the output
                 const float l_row = l_s[row] + l_s[128 + row];
                 // causal rows that saw no key have l = 0 and RO = 0: write zeros
                 const float rl = (kCausal && l_row == 0.f) ? 0.f : __frcp_rn(l_row);
+                if (kCkpt && half == 0) p.ck.recip[row] = rl;
                 const int r = q0 + row;
                 if (r < lq) {
                     uint4* dst = reinterpret_cast<uint4*>(p.o + b * p.osb + h * p.osh + (int64_t)r * p.osn +
@@ -621,7 +646,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
 }
 
-template <int D, bool kCapture, bool kCausal, bool kFusedQ = false>
+template <int D, bool kCapture, bool kCausal, bool kFusedQ = false, bool kCkpt = false>
 cudaError_t launch_one(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, cudaStream_t s) {
     static bool attr_set[64] = {};                          // per device, per instantiation
@@ -630,13 +655,13 @@ cudaError_t launch_one(const AttnParams& p, const CUtensorMap& tq, const CUtenso
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(sage_attn_kernel<D, kCapture, kCausal, kFusedQ>,
+        cudaError_t e = cudaFuncSetAttribute(sage_attn_kernel<D, kCapture, kCausal, kFusedQ, kCkpt>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    dim3 grid((unsigned)((p.Nq + 127) / 128), (unsigned)p.H, (unsigned)p.B);
-    sage_attn_kernel<D, kCapture, kCausal, kFusedQ><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+    const dim3 grid = kCkpt ? dim3(1, 1, 1) : dim3((unsigned)((p.Nq + 127) / 128), (unsigned)p.H, (unsigned)p.B);
+    sage_attn_kernel<D, kCapture, kCausal, kFusedQ, kCkpt><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 
@@ -658,6 +683,17 @@ cudaError_t launch_attn(const AttnParams& p, const CUtensorMap& tq, const CUtens
     *launches = 1;
     if (p.D == 128) return launch_d<128>(p, tq, tk, tv, capture, causal, fused_q, s);
     if (p.D == 64) return launch_d<64>(p, tq, tk, tv, capture, causal, fused_q, s);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attn_checkpoints(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                                    const CUtensorMap& tv, bool causal, cudaStream_t s) {
+    if (p.D == 128)
+        return causal ? launch_one<128, false, true, false, true>(p, tq, tk, tv, s)
+                      : launch_one<128, false, false, false, true>(p, tq, tk, tv, s);
+    if (p.D == 64)
+        return causal ? launch_one<64, false, true, false, true>(p, tq, tk, tv, s)
+                      : launch_one<64, false, false, false, true>(p, tq, tk, tv, s);
     return cudaErrorInvalidValue;
 }
 

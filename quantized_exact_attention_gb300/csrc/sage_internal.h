@@ -43,6 +43,18 @@ struct PrepParams {
     float* v_inv;                          // workspace [B,H,D]
 };
 
+// Stage checkpoints of one query tile (see sage_attn_checkpoints).
+struct CkptParams {
+    float* m;          // [T][128]        running max after tile t
+    float* l;          // [T][2][128]     each half row's running sum after tile t
+    float* alpha;      // [T][128]        rescale factor of tile t
+    uint8_t* p8;       // [T][128][128]   e4m3 P bytes of tile t (row-major, key fastest)
+    uint16_t* pv16;    // [T][128][D]     FP16 PV tile sums
+    float* ro;         // [T][128][D]     FP32 running output after tile t
+    float* recip;      // [128]           1/l
+    int b, h, qtile;   // the query tile (its CTA is the only one launched)
+};
+
 struct AttnParams {
     const float* q_scale;
     const float* k_scale;
@@ -58,6 +70,7 @@ struct AttnParams {
     int* status;                           // device status words
     int fault_mode;                        // test hook: 0 = none
     float* q_scale_out;                    // fused Q only: per-block Q scales written by the kernel
+    CkptParams ck;                         // checkpoint kernel only
 };
 
 // Device status word layout: [0] first error code, [1] block id, [2] role, [3] tile.
@@ -72,5 +85,9 @@ cudaError_t launch_prep(const PrepParams& p, bool with_q, cudaStream_t s, int* l
 cudaError_t launch_attn(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                         const CUtensorMap& tv, bool capture, bool causal, bool fused_q, cudaStream_t s,
                         int* launches);
+// One CTA (p.ck.b, p.ck.h, p.ck.qtile) of the attention kernel, writing its
+// stage checkpoints besides its output rows.
+cudaError_t launch_attn_checkpoints(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                                    const CUtensorMap& tv, bool causal, cudaStream_t s);
 
 }  // namespace sage
