@@ -17,7 +17,7 @@ PV, FP32 RO, reciprocal, final BF16 output; "Phase 1 State-Ownership
 Decision": strict tile order, exact FP8 score bytes, per-tile RO rescaling).
 
 The pages give the stages but none of their constants.  Every constant,
-granularity and rounding choice below is a reading, tagged R1..R14 and listed
+granularity and rounding choice below is a reading, tagged R1..R16 and listed
 with its justification in the design notes:
 
   R3  K channel mean: FP32, chunks of 64 valid tokens summed in ascending
@@ -42,6 +42,10 @@ with its justification in the design notes:
       row that sees no key is zero, as in R14.  A tile whose keys are all
       hidden from a row changes nothing for it (alpha = exp2(0) = 1, p = 0),
       so the row's result is the non-causal one over its visible prefix.
+  R16 a second contract variant with BKV = 64 (the pages' 64-key epochs):
+      the online-softmax tile and the inner PV sum cover 64 keys and
+      S_V = 144/64 = 2.25, so the FP16 bound BKV * S_P * S_V <= 65504 holds
+      at the same margin.  Q/K blocks are unchanged.
 
 Precision: every step is carried out in the precision the contract names
 (FP32 via numpy float32 arithmetic, which rounds each operation to nearest
@@ -218,14 +222,16 @@ def quantize_int8_blocks(x: np.ndarray, valid: int, block: int):
     return codes, scales
 
 
-def quantize_v_fp8(v: np.ndarray, valid: int):
+def quantize_v_fp8(v: np.ndarray, valid: int, s_v: float | None = None):
     """Per-channel FP8 e4m3 quantization of one head's values (R6).
 
     v: float32 [N, D].  Per channel d over the valid rows: amax = max |v|,
     v_scale = amax / S_V, code = e4m3_rne_satfinite(v * (S_V / amax)).
     Rows [valid, N) get code 0; channels with amax = 0 get scale 0, codes 0.
+    s_v: the target magnitude S_V (default: the BKV = 128 contract's).
     Returns (codes uint8 [N, D], v_scale float32 [D]).
     """
+    s_v = S_V if s_v is None else s_v
     n, d = v.shape
     codes = np.zeros((n, d), dtype=np.uint8)
     scale = np.zeros(d, dtype=F32)
@@ -235,8 +241,8 @@ def quantize_v_fp8(v: np.ndarray, valid: int):
     amax = np.max(np.abs(vv), axis=0).astype(F32)
     nz = amax > 0
     safe = np.where(nz, amax, F32(1.0)).astype(F32)
-    inv = (F32(S_V) / safe).astype(F32)
-    scale = np.where(nz, (amax / F32(S_V)).astype(F32), F32(0.0)).astype(F32)
+    inv = (F32(s_v) / safe).astype(F32)
+    scale = np.where(nz, (amax / F32(s_v)).astype(F32), F32(0.0)).astype(F32)
     scaled = (vv * inv[None, :]).astype(F32)
     c = e4m3_encode(scaled)
     codes[:valid] = np.where(nz[None, :], c, np.uint8(0))
@@ -255,15 +261,19 @@ class Prepared:
     k_mean: np.ndarray    # f32   [B, H, D]
     q_len: np.ndarray     # int   [B]
     kv_len: np.ndarray    # int   [B]
+    bkv: int = 128        # keys per online-softmax tile / inner PV sum (R9, R16)
 
 
 def prepare(q: np.ndarray, k: np.ndarray, v: np.ndarray, q_len=None, kv_len=None,
-            smooth_k: bool = True) -> Prepared:
+            smooth_k: bool = True, bkv: int | None = None) -> Prepared:
     """Quantize float32 [B, H, N, D] Q/K/V (values exactly representable in BF16).
 
     smooth_k=False skips the K mean subtraction (used only to show what the
-    smoothing step buys; the contract always smooths).
+    smoothing step buys; the contract always smooths).  bkv: the contract's
+    KV tile (128, or 64 for R16); S_V scales inversely with it.
     """
+    bkv = BKV if bkv is None else int(bkv)
+    s_v = S_V * BKV / bkv
     B, H, Nq, D = q.shape
     Nkv = k.shape[2]
     q_len = np.full(B, Nq) if q_len is None else np.asarray(q_len)
@@ -286,8 +296,8 @@ def prepare(q: np.ndarray, k: np.ndarray, v: np.ndarray, q_len=None, kv_len=None
             km[b, h] = means[h]
             ksm = (kf_all[h] - means[h][None, :]).astype(F32)
             k8[b, h], ks[b, h] = quantize_int8_blocks(ksm, lk, BKS)
-            v8[b, h], vs[b, h] = quantize_v_fp8(vf, lk)
-    return Prepared(q8, k8, v8, qs, ks, vs, km, q_len, kv_len)
+            v8[b, h], vs[b, h] = quantize_v_fp8(vf, lk, s_v)
+    return Prepared(q8, k8, v8, qs, ks, vs, km, q_len, kv_len, bkv)
 
 
 # ---------------------------------------------------------------------------
@@ -364,8 +374,9 @@ def attention_rows(prep: Prepared, b: int, h: int, rows: np.ndarray,
     m = np.full(nr, -np.inf, dtype=F32)
     l = np.zeros(nr, dtype=F32)
     ro = np.zeros((nr, D), dtype=F32)
-    for j0 in range(0, lk, BKV):                                # strict ascending tile order
-        j1 = min(j0 + BKV, lk)
+    bkv = prep.bkv
+    for j0 in range(0, lk, bkv):                                # strict ascending tile order
+        j1 = min(j0 + bkv, lk)
         cols = np.arange(j0, j1)
         k_sc = prep.k_scale[b, h][cols // BKS]                  # [w]
         f = ((q_sc[:, None] * k_sc[None, :]).astype(F32) * c).astype(F32)

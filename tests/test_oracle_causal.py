@@ -109,3 +109,48 @@ def test_d64_single_key_gives_dequantized_value_row():
         exact = _dequant_v(prep, 0, h, 1)[0]
         ulp = np.spacing(np.abs(exact).astype(np.float32)).astype(np.float64) * 2 ** 16
         assert np.all(np.abs(out[0, h] - exact[None, :]) <= ulp[None, :])
+
+
+# --- BKV = 64 contract variant (R16) ------------------------------------------
+@pytest.mark.parametrize("cfg", [2, 3])
+def test_bkv64_close_to_fp64_attention(cfg):
+    w = W.make_config(cfg)
+    if cfg == 3:
+        w = W.make_custom(B=2, H=3, Nq=500, Nkv=500, seed=49, k_offset_std=2.0, q_len=[500, 301],
+                          kv_len=[500, 377])
+    q, k, v = _logical(w)
+    prep = O.prepare(q, k, v, w.q_len, w.kv_len, bkv=64)
+    out = O.bf16_bits_to_f32(O.attention(prep))
+    for b in range(w.B):
+        lq, lk = w.qlens[b], w.kvlens[b]
+        cos, rel = _metrics(out[b:b + 1, :, :lq], fp64_attention(q[b:b + 1, :, :lq], k[b:b + 1, :, :lk],
+                                                                  v[b:b + 1, :, :lk]))
+        assert cos >= 0.999 and rel <= 5e-2
+
+
+def test_bkv64_v_scale_and_tiles():
+    # S_V doubles with half the tile; every V code then covers |v| <= 2.25
+    w = W.make_custom(B=1, H=1, Nq=128, Nkv=300, seed=50)
+    q, k, v = _logical(w)
+    p128, p64 = O.prepare(q, k, v), O.prepare(q, k, v, bkv=64)
+    assert np.array_equal(p128.v_scale.view(np.uint32), (p64.v_scale * F32(2)).view(np.uint32))
+    assert np.abs(O.e4m3_decode(p64.v8)).max() <= 2.25
+    assert np.array_equal(p128.q8, p64.q8) and np.array_equal(p128.k8, p64.k8)
+    ck = O.Checkpoints()
+    O.attention_rows(p64, 0, 0, np.arange(128), checkpoints=ck)
+    assert len(ck.m) == 5                                      # ceil(300 / 64) tiles
+    assert max(np.abs(pv).max() for pv in ck.pv16) <= 64 * 448 * 2.25
+    assert np.all((ck.p8[0] == 0x7E).any(axis=1))             # p = 1 at each row's first-tile max
+
+
+def test_bkv64_single_key_gives_dequantized_value_row():
+    rng = np.random.default_rng(51)
+    q = rng.standard_normal((1, 2, 70, 128)).astype(F32)
+    k = rng.standard_normal((1, 2, 1, 128)).astype(F32)
+    v = rng.standard_normal((1, 2, 1, 128)).astype(F32)
+    prep = O.prepare(q, k, v, bkv=64)
+    out = O.bf16_bits_to_f32(O.attention(prep))
+    for h in range(2):
+        exact = _dequant_v(prep, 0, h, 1)[0]
+        ulp = np.spacing(np.abs(exact).astype(np.float32)).astype(np.float64) * 2 ** 16
+        assert np.all(np.abs(out[0, h] - exact[None, :]) <= ulp[None, :])

@@ -30,6 +30,12 @@ def _ties_away(x):
 
 
 _VISIBLE = O.visible_keys
+_QUANT_V = O.quantize_v_fp8
+
+
+def _v_scale_ignores_tile(v, valid, s_v=None):
+    # the BKV = 64 variant quantizing V with the BKV = 128 target magnitude
+    return _QUANT_V(v, valid, None)
 
 
 def _causal_top_left(prep, b, rows, causal):
@@ -78,6 +84,9 @@ MUTATIONS = {
     "causal_diagonal_key_hidden": (
         lambda mp: mp.setattr(O, "visible_keys", _causal_strict),
         TC.test_causal_first_row_is_its_first_value),
+    "bkv64_keeps_bkv128_v_scale": (
+        lambda mp: mp.setattr(O, "quantize_v_fp8", _v_scale_ignores_tile),
+        TC.test_bkv64_v_scale_and_tiles),
     "kv_tile_256": (
         lambda mp: mp.setattr(O, "BKV", 256),
         TA.test_checkpoints_follow_online_softmax_invariants),
