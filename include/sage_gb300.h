@@ -167,6 +167,24 @@ int sage_qk_int32(const sage_prep_buffers* in, int32_t* s,
                   int B, int H, int Nq, int Nkv, int D,
                   const int32_t* q_len, const int32_t* kv_len, void* stream);
 
+/* The BKV = 64 form of the contract, matching the 64-key epochs of Experiment
+ * Log, "Phase 2A" (64-key K/V slots): the online-softmax tile and the inner
+ * FP16 PV sum cover 64 keys, and V is quantized to |v| <= S_V = 144/64 = 2.25
+ * so that 64 * 448 * S_V stays within the FP16 range.  bkv = 128 gives the
+ * default contract (identical to sage_prep_qkv / sage_attn_fwd[_causal]);
+ * any other value returns SAGE_ERR_UNSUPPORTED.  Prepare and attend with the
+ * same bkv: only V's codes and scales depend on it.  Other arguments,
+ * layouts and errors as for sage_prep_qkv and sage_attn_fwd; causal as for
+ * sage_attn_fwd_causal. */
+int sage_prep_qkv_bkv(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
+                      int B, int H, int Nq, int Nkv, int D,
+                      const int32_t* q_len, const int32_t* kv_len, int bkv,
+                      const sage_prep_buffers* out, void* stream);
+int sage_attn_fwd_bkv(const sage_prep_buffers* in, const sage_tensor* o,
+                      int B, int H, int Nq, int Nkv, int D,
+                      const int32_t* q_len, const int32_t* kv_len, float sm_scale,
+                      int bkv, int causal, void* stream);
+
 /* Stage checkpoints of one query tile (device buffers, caller-owned).  T is
  * the number of 128-key tiles the tile visits: ceil(kv_len/128), or up to its
  * diagonal for the causal form; size every buffer for T = ceil(Nkv/128).

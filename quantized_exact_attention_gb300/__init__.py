@@ -30,7 +30,7 @@ HEAD_DIMS = (64, 128)       # head dimensions the kernels are built for
 
 # Names the header declares (checked by the CPU tests against the .so exports).
 EXPORTED = ("sage_buffer_sizes", "sage_prep_qkv", "sage_attn_fwd", "sage_attn_fwd_causal", "sage_attention",
-            "sage_attn_checkpoints", "sage_qk_int32",
+            "sage_attn_checkpoints", "sage_prep_qkv_bkv", "sage_attn_fwd_bkv", "sage_qk_int32",
             "sage_attention_host", "sage_get_device_status", "sage_status_string",
             "sage_last_launch_count", "sage_debug_inject_fault", "sage_prep_qkv_noalloc",
             "sage_prep_noalloc_capacity")
@@ -87,6 +87,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                   P(sage_prep_buffers), vp]
     lib.sage_attn_fwd.argtypes = [P(sage_prep_buffers), P(sage_tensor), i, i, i, i, i, vp, vp, f, vp]
     lib.sage_attn_fwd_causal.argtypes = lib.sage_attn_fwd.argtypes
+    lib.sage_prep_qkv_bkv.argtypes = [P(sage_tensor), P(sage_tensor), P(sage_tensor), i, i, i, i, i, vp, vp, i,
+                                      P(sage_prep_buffers), vp]
+    lib.sage_attn_fwd_bkv.argtypes = [P(sage_prep_buffers), P(sage_tensor), i, i, i, i, i, vp, vp, f, i, i, vp]
     lib.sage_attn_checkpoints.argtypes = [P(sage_prep_buffers), P(sage_tensor), i, i, i, i, i, vp, vp, f, i,
                                           i, i, i, P(sage_checkpoints), vp]
     lib.sage_attention.argtypes = [P(sage_tensor), P(sage_tensor), P(sage_tensor), P(sage_tensor),
@@ -183,13 +186,19 @@ def _lens(x):
     return x.data_ptr()
 
 
-def sage_prep_qkv(q, k, v, bufs: PrepBuffers, q_len=None, kv_len=None, stream=None):
-    """Enqueue the preparation kernels on [B,H,N,D] BF16 views q, k, v."""
+def sage_prep_qkv(q, k, v, bufs: PrepBuffers, q_len=None, kv_len=None, stream=None, bkv: int = 128):
+    """Enqueue the preparation kernels on [B,H,N,D] BF16 views q, k, v.
+    bkv = 64 prepares for the BKV = 64 contract (sage_prep_qkv_bkv)."""
     B, H, Nq, D = q.shape
     Nkv = k.shape[2]
     qs, ks, vs, pb = tensor_desc(q), tensor_desc(k), tensor_desc(v), bufs.c_struct()
-    rc = load_library().sage_prep_qkv(ctypes.byref(qs), ctypes.byref(ks), ctypes.byref(vs), B, H, Nq, Nkv, D,
-                                      _lens(q_len), _lens(kv_len), ctypes.byref(pb), _stream_ptr(stream))
+    lib = load_library()
+    if bkv == 128:
+        rc = lib.sage_prep_qkv(ctypes.byref(qs), ctypes.byref(ks), ctypes.byref(vs), B, H, Nq, Nkv, D,
+                               _lens(q_len), _lens(kv_len), ctypes.byref(pb), _stream_ptr(stream))
+    else:
+        rc = lib.sage_prep_qkv_bkv(ctypes.byref(qs), ctypes.byref(ks), ctypes.byref(vs), B, H, Nq, Nkv, D,
+                                   _lens(q_len), _lens(kv_len), int(bkv), ctypes.byref(pb), _stream_ptr(stream))
     _check(rc, "sage_prep_qkv")
 
 
@@ -210,14 +219,20 @@ def sage_prep_noalloc_capacity() -> int:
 
 
 def sage_attn_fwd(bufs: PrepBuffers, o, q_len=None, kv_len=None, sm_scale: float = 0.0, stream=None,
-                  Nkv: int | None = None, causal: bool = False):
+                  Nkv: int | None = None, causal: bool = False, bkv: int = 128):
     """Enqueue the fused attention kernel; o is a [B,H,Nq,D] BF16 view.
     causal=True calls sage_attn_fwd_causal (key j visible to query i iff
-    j <= i + kv_len - q_len)."""
+    j <= i + kv_len - q_len); bkv = 64 calls sage_attn_fwd_bkv."""
     B, H, Nq, D = o.shape
     Nkv = bufs.k16.shape[2] if Nkv is None else Nkv
     os_, pb = tensor_desc(o), bufs.c_struct()
     lib = load_library()
+    if bkv != 128:
+        rc = lib.sage_attn_fwd_bkv(ctypes.byref(pb), ctypes.byref(os_), B, H, Nq, Nkv, D, _lens(q_len),
+                                   _lens(kv_len), float(sm_scale), int(bkv), 1 if causal else 0,
+                                   _stream_ptr(stream))
+        _check(rc, "sage_attn_fwd_bkv")
+        return
     fn = lib.sage_attn_fwd_causal if causal else lib.sage_attn_fwd
     rc = fn(ctypes.byref(pb), ctypes.byref(os_), B, H, Nq, Nkv, D,
             _lens(q_len), _lens(kv_len), float(sm_scale), _stream_ptr(stream))

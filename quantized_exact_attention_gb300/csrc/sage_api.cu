@@ -148,9 +148,9 @@ int sage_buffer_sizes(int B, int H, int Nq, int Nkv, int D, sage_sizes* out) {
     return SAGE_OK;
 }
 
-int sage_prep_qkv(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v, int B, int H, int Nq,
-                  int Nkv, int D, const int32_t* q_len, const int32_t* kv_len, const sage_prep_buffers* out,
-                  void* stream) {
+static int prep_common(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v, int B, int H, int Nq,
+                       int Nkv, int D, const int32_t* q_len, const int32_t* kv_len, float sv,
+                       const sage_prep_buffers* out, void* stream) {
     int rc = check_shape(B, H, Nq, Nkv, D);
     if (rc != SAGE_OK) return rc;
     if ((rc = check_tensor(q)) != SAGE_OK || (rc = check_tensor(k)) != SAGE_OK || (rc = check_tensor(v)) != SAGE_OK)
@@ -166,7 +166,7 @@ int sage_prep_qkv(const sage_tensor* q, const sage_tensor* k, const sage_tensor*
     p.qsb = q->stride_b; p.qsh = q->stride_h; p.qsn = q->stride_n;
     p.ksb = k->stride_b; p.ksh = k->stride_h; p.ksn = k->stride_n;
     p.vsb = v->stride_b; p.vsh = v->stride_h; p.vsn = v->stride_n;
-    p.B = B; p.H = H; p.Nq = Nq; p.Nkv = Nkv; p.D = D;
+    p.B = B; p.H = H; p.Nq = Nq; p.Nkv = Nkv; p.D = D; p.sv = sv;
     p.nkv_pad = (int)sz.nkv_pad;
     p.nq_blocks = (int)ceil_div(Nq, kBQS);
     p.nk_blocks = (int)ceil_div(Nkv, kBKS);
@@ -186,9 +186,27 @@ int sage_prep_qkv(const sage_tensor* q, const sage_tensor* k, const sage_tensor*
     return rc;
 }
 
+// S_V of the BKV contract (R6): 144 / BKV; 0 for an unsupported tile length.
+static float sv_of_bkv(int bkv) { return bkv == 128 ? kSV : (bkv == 64 ? 2.0f * kSV : 0.f); }
+
+int sage_prep_qkv(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v, int B, int H, int Nq,
+                  int Nkv, int D, const int32_t* q_len, const int32_t* kv_len, const sage_prep_buffers* out,
+                  void* stream) {
+    return prep_common(q, k, v, B, H, Nq, Nkv, D, q_len, kv_len, kSV, out, stream);
+}
+
+int sage_prep_qkv_bkv(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v, int B, int H, int Nq,
+                      int Nkv, int D, const int32_t* q_len, const int32_t* kv_len, int bkv,
+                      const sage_prep_buffers* out, void* stream) {
+    const float sv = sv_of_bkv(bkv);
+    if (sv == 0.f) return SAGE_ERR_UNSUPPORTED;
+    return prep_common(q, k, v, B, H, Nq, Nkv, D, q_len, kv_len, sv, out, stream);
+}
+
 static int attn_common(const sage_prep_buffers* in, const sage_tensor* o, int32_t* s_out, int B, int H, int Nq,
                        int Nkv, int D, const int32_t* q_len, const int32_t* kv_len, float sm_scale,
-                       void* stream, bool capture, bool causal, const CkptParams* ck = nullptr) {
+                       void* stream, bool capture, bool causal, const CkptParams* ck = nullptr,
+                       bool bkv64 = false) {
     int rc = check_shape(B, H, Nq, Nkv, D);
     if (rc != SAGE_OK) return rc;
     sage_sizes sz;
@@ -237,8 +255,11 @@ static int attn_common(const sage_prep_buffers* in, const sage_tensor* o, int32_
         rc = status_from(launch_attn_checkpoints(p, tq, tk, tv, causal, static_cast<cudaStream_t>(stream)));
         launches = 1;
     } else {
-        rc = status_from(launch_attn(p, tq, tk, tv, capture, causal, false, static_cast<cudaStream_t>(stream),
-                                     &launches));
+        AttnMode mode;
+        mode.capture = capture;
+        mode.causal = causal;
+        mode.bkv64 = bkv64;
+        rc = status_from(launch_attn(p, tq, tk, tv, mode, static_cast<cudaStream_t>(stream), &launches));
     }
     if (rc == SAGE_OK) g_last_launches = launches;
     return rc;
@@ -252,6 +273,14 @@ int sage_attn_fwd(const sage_prep_buffers* in, const sage_tensor* o, int B, int 
 int sage_attn_fwd_causal(const sage_prep_buffers* in, const sage_tensor* o, int B, int H, int Nq, int Nkv, int D,
                          const int32_t* q_len, const int32_t* kv_len, float sm_scale, void* stream) {
     return attn_common(in, o, nullptr, B, H, Nq, Nkv, D, q_len, kv_len, sm_scale, stream, false, true);
+}
+
+int sage_attn_fwd_bkv(const sage_prep_buffers* in, const sage_tensor* o, int B, int H, int Nq, int Nkv, int D,
+                      const int32_t* q_len, const int32_t* kv_len, float sm_scale, int bkv, int causal,
+                      void* stream) {
+    if (bkv != 64 && bkv != 128) return SAGE_ERR_UNSUPPORTED;
+    return attn_common(in, o, nullptr, B, H, Nq, Nkv, D, q_len, kv_len, sm_scale, stream, false, causal != 0,
+                       nullptr, bkv == 64);
 }
 
 int sage_attn_checkpoints(const sage_prep_buffers* in, const sage_tensor* o, int B, int H, int Nq, int Nkv, int D,
@@ -304,7 +333,7 @@ int sage_attention(const sage_tensor* q, const sage_tensor* k, const sage_tensor
     pp.v = static_cast<const uint16_t*>(v->ptr);
     pp.ksb = k->stride_b; pp.ksh = k->stride_h; pp.ksn = k->stride_n;
     pp.vsb = v->stride_b; pp.vsh = v->stride_h; pp.vsn = v->stride_n;
-    pp.B = B; pp.H = H; pp.Nq = Nq; pp.Nkv = Nkv; pp.D = D;
+    pp.B = B; pp.H = H; pp.Nq = Nq; pp.Nkv = Nkv; pp.D = D; pp.sv = kSV;
     pp.nkv_pad = (int)sz.nkv_pad;
     pp.nq_blocks = (int)ceil_div(Nq, kBQS);
     pp.nk_blocks = (int)ceil_div(Nkv, kBKS);
@@ -345,7 +374,10 @@ int sage_attention(const sage_tensor* q, const sage_tensor* k, const sage_tensor
     p.fault_mode = fault_mode_for_next_launch;
     fault_mode_for_next_launch = 0;
     int launches = 0;
-    rc = status_from(launch_attn(p, tq, tk, tv, false, causal != 0, true, s, &launches));
+    AttnMode mode;
+    mode.causal = causal != 0;
+    mode.fused_q = true;
+    rc = status_from(launch_attn(p, tq, tk, tv, mode, s, &launches));
     if (rc == SAGE_OK) g_last_launches = launches + prep_launches;
     return rc;
 }

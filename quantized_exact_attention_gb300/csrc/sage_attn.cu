@@ -88,8 +88,8 @@ struct Smem {
     static constexpr uint32_t OFF_K = OFF_Q + kTileQBytes;
     static constexpr uint32_t OFF_V = OFF_K + kNK * kTileKBytes;
     static constexpr uint32_t OFF_BAR = OFF_V + kNV * kTileVBytes;
-    static constexpr uint32_t OFF_ALPHA = OFF_BAR + ((B_COUNT * 8 + 15) / 16) * 16;   // float [2][128]
-    static constexpr uint32_t OFF_XM = OFF_ALPHA + 2 * 128 * 4;                       // float [2 buf][2 half][128]
+    static constexpr uint32_t OFF_ALPHA = OFF_BAR + ((B_COUNT * 8 + 15) / 16) * 16;   // float [2 buf][2 epoch][128]
+    static constexpr uint32_t OFF_XM = OFF_ALPHA + 4 * 128 * 4;                       // float [2 buf][2 half][128]
     static constexpr uint32_t OFF_L = OFF_XM + 4 * 128 * 4;                           // float [2 half][128]
     static constexpr uint32_t OFF_VS = OFF_L + 2 * 128 * 4;                           // float [D]
     static constexpr uint32_t OFF_TMEM = OFF_VS + 128 * 4;                            // u32
@@ -146,7 +146,11 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
 // kCkpt: a single CTA (p.ck.b, p.ck.h, p.ck.qtile) also writes its per-tile
 // stage values (running max, rescale, running sums, P bytes, FP16 PV sums,
 // FP32 running output, reciprocal) to p.ck.
-template <int D, bool kCapture, bool kCausal, bool kFusedQ, bool kCkpt = false>
+// kB64: the BKV = 64 contract.  Each 128-key S tile is two online-softmax
+// epochs: keys 0-63 (half 0) then keys 64-127 (half 1), each with its own
+// running maximum, rescale and FP16 PV sum (two PV groups of K = 64 through
+// the one PV accumulator) and its own RO update.
+template <int D, bool kCapture, bool kCausal, bool kFusedQ, bool kCkpt = false, bool kB64 = false>
 __global__ void __launch_bounds__(kThreads, 1)
 sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
@@ -362,12 +366,24 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 break;
             }
             tc_fence_after();
-            float m_new = fmaxf(m_run, fmaxf(xm[(sb * 2 + 0) * 128 + row], xm[(sb * 2 + 1) * 128 + row]));
+            const float mt_a = xm[(sb * 2 + 0) * 128 + row], mt_b = xm[(sb * 2 + 1) * 128 + row];
+            float m_new = fmaxf(m_run, fmaxf(mt_a, mt_b));
             // causal: a row that has seen no key yet keeps m = -inf; measure from
             // 0 so that alpha = 0 and every p = 0 instead of NaN
             if (kCausal && m_new == -INFINITY) m_new = 0.f;
-            const float alpha = ex2_approx(m_run - m_new);  // first tile: 2^-inf = 0
-            const float nb = kLog2SP - m_new;               // P is produced pre-scaled by 448
+            float alpha = ex2_approx(m_run - m_new);        // first tile: 2^-inf = 0
+            float nb = kLog2SP - m_new;                     // P is produced pre-scaled by 448
+            float alpha_b = 1.f;                            // kB64: rescale of the second epoch
+            if constexpr (kB64) {
+                // epoch A (keys 0-63) ends at mA = max(m, max_A), epoch B
+                // (keys 64-127) at m_new = max(mA, max_B)
+                float m_a = fmaxf(m_run, mt_a);
+                const bool none_a = kCausal && (m_a == -INFINITY);
+                if (none_a) m_a = 0.f;
+                alpha = ex2_approx(m_run - m_a);
+                alpha_b = none_a ? 0.f : ex2_approx(m_a - m_new);
+                nb = kLog2SP - (half == 0 ? m_a : m_new);
+            }
 
             uint32_t pk[16];
             float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
@@ -412,12 +428,19 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     ok = false;
                     break;
                 }
-                alpha_s[sb * 128 + row] = alpha;
+                alpha_s[(sb * 2) * 128 + row] = alpha;
+                if (kB64) alpha_s[(sb * 2 + 1) * 128 + row] = alpha_b;
             }
             tc_fence_before();
             mbar_arrive(bar(B_PFULL + s3));
             if (half == 0) mbar_arrive(bar(B_AFULL + sb));
-            l_run = fmaf(l_run, alpha, tile_sum);
+            if constexpr (kB64) {
+                // half 0's keys join in epoch A, half 1's in epoch B
+                l_run = half == 0 ? __fmul_rn(fmaf(l_run, alpha, tile_sum), alpha_b)
+                                  : fmaf(__fmul_rn(l_run, alpha), alpha_b, tile_sum);
+            } else {
+                l_run = fmaf(l_run, alpha, tile_sum);
+            }
             m_run = (kCausal && l_run == 0.f) ? -INFINITY : m_new;
             if constexpr (kCkpt) p.ck.l[(t * 2 + half) * 128 + row] = l_run;
         }
@@ -444,39 +467,45 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     ok = false;
                     break;
                 }
-                const float alpha = alpha_s[sb * 128 + row];
+                const float alpha_a = alpha_s[(sb * 2) * 128 + row];
+                const float alpha_b = kB64 ? alpha_s[(sb * 2 + 1) * 128 + row] : 1.f;
                 mbar_arrive(bar(B_AFREE + sb));
-                const bool unit = __all_sync(0xffffffffu, alpha == 1.0f);   // RN(RO * 1) == RO
-                if (!warp_wait(bar(B_PVFULL), t & 1, abort_flag)) {
-                    if (lane == 0) record_failure(p, abort_flag, R_CORRECT, t);
-                    ok = false;
-                    break;
+#pragma unroll 1
+                for (int e = 0; e < (kB64 ? 2 : 1); ++e) {  // PV epochs of this tile
+                    const float alpha = e ? alpha_b : alpha_a;
+                    const bool unit = __all_sync(0xffffffffu, alpha == 1.0f);   // RN(RO * 1) == RO
+                    if (!warp_wait(bar(B_PVFULL), kB64 ? e : (t & 1), abort_flag)) {
+                        if (lane == 0) record_failure(p, abort_flag, R_CORRECT, t);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < kDH / 32; ++c) {
+                        uint32_t v[16];                         // FP16 tile sums, two per register
+                        tmem_ld32_pack16(tmem + lane_base + TM_PV + half * kDH + c * 32, v);
+                        tmem_wait_ld();
+                        if (c == kDH / 32 - 1) {
+                            tc_fence_before();
+                            mbar_arrive(bar(B_PVFREE));
+                        }
+                        if constexpr (kCkpt) {
+                            uint4* dp = reinterpret_cast<uint4*>(p.ck.pv16 + ((int64_t)t * 128 + row) * D + half * kDH +
+                                                                 c * 32);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) dp[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                        }
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            // RO = RN(RN(RO * alpha) + PV16)
+                            float& r0 = ro[c * 32 + 2 * i];
+                            float& r1 = ro[c * 32 + 2 * i + 1];
+                            if (!unit) mul2_s(r0, r1, alpha);
+                            add_f16x2_to(r0, r1, v[i]);
+                        }
+                    }
                 }
-                tc_fence_after();
-#pragma unroll
-                for (int c = 0; c < kDH / 32; ++c) {
-                    uint32_t v[16];                         // FP16 tile sums, two per register
-                    tmem_ld32_pack16(tmem + lane_base + TM_PV + half * kDH + c * 32, v);
-                    tmem_wait_ld();
-                    if (c == kDH / 32 - 1) {
-                        tc_fence_before();
-                        mbar_arrive(bar(B_PVFREE));
-                    }
-                    if constexpr (kCkpt) {
-                        uint4* dp = reinterpret_cast<uint4*>(p.ck.pv16 + ((int64_t)t * 128 + row) * D + half * kDH +
-                                                             c * 32);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) dp[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-                    }
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        // RO = RN(RN(RO * alpha) + PV16)
-                        float& r0 = ro[c * 32 + 2 * i];
-                        float& r1 = ro[c * 32 + 2 * i + 1];
-                        if (!unit) mul2_s(r0, r1, alpha);
-                        add_f16x2_to(r0, r1, v[i]);
-                    }
-                }
+                if (!ok) break;
                 if constexpr (kCkpt) {
                     float4* dp = reinterpret_cast<float4*>(p.ck.ro + ((int64_t)t * 128 + row) * D + half * kDH);
 #pragma unroll
@@ -608,15 +637,23 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // that only the wait for P sits between the softmax and the PV MMA.
             auto issue_pv = [&](int t) -> bool {
                 if (!mbar_wait(bar(B_VFULL + v_st), v_ph, abort_flag)) return false;
-                if (t >= 1 && !mbar_wait(bar(B_PVFREE), (t - 1) & 1, abort_flag)) return false;
-                if (!mbar_wait(bar(B_PFULL + pb), pph, abort_flag)) return false;
-                tc_fence_after();
                 const uint64_t bV = dV + (uint64_t)(v_st * (kTileVBytes >> 4));
                 const uint32_t aP = tmem + TM_S + pb * 128;
+                constexpr int kEpochs = kB64 ? 2 : 1, kSteps = 4 / kEpochs;   // K = 32 steps per epoch
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_f8_ts(tmem + TM_PV, aP + kk * 8, bV + (uint64_t)(kk * (32 >> 4)), kIdescPV, kk > 0 ? 1u : 0u);
-                mma_commit(bar(B_PVFULL));
+                for (int e = 0; e < kEpochs; ++e) {
+                    const int n = t * kEpochs + e;                           // PV accumulator use
+                    if (n >= 1 && !mbar_wait(bar(B_PVFREE), (n - 1) & 1, abort_flag)) return false;
+                    if (e == 0 && !mbar_wait(bar(B_PFULL + pb), pph, abort_flag)) return false;
+                    tc_fence_after();
+#pragma unroll
+                    for (int j = 0; j < kSteps; ++j) {
+                        const int kk = e * kSteps + j;
+                        mma_f8_ts(tmem + TM_PV, aP + kk * 8, bV + (uint64_t)(kk * (32 >> 4)), kIdescPV,
+                                  j > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar(B_PVFULL));
+                }
                 mma_commit(bar(B_VEMPTY + v_st));
                 if (++v_st == kNV) { v_st = 0; v_ph ^= 1; }
                 if (++pb == kNS) { pb = 0; pph ^= 1; }
@@ -646,7 +683,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
 }
 
-template <int D, bool kCapture, bool kCausal, bool kFusedQ = false, bool kCkpt = false>
+template <int D, bool kCapture, bool kCausal, bool kFusedQ = false, bool kCkpt = false, bool kB64 = false>
 cudaError_t launch_one(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, cudaStream_t s) {
     static bool attr_set[64] = {};                          // per device, per instantiation
@@ -655,34 +692,38 @@ cudaError_t launch_one(const AttnParams& p, const CUtensorMap& tq, const CUtenso
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(sage_attn_kernel<D, kCapture, kCausal, kFusedQ, kCkpt>,
+        cudaError_t e = cudaFuncSetAttribute(sage_attn_kernel<D, kCapture, kCausal, kFusedQ, kCkpt, kB64>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
     const dim3 grid = kCkpt ? dim3(1, 1, 1) : dim3((unsigned)((p.Nq + 127) / 128), (unsigned)p.H, (unsigned)p.B);
-    sage_attn_kernel<D, kCapture, kCausal, kFusedQ, kCkpt><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+    sage_attn_kernel<D, kCapture, kCausal, kFusedQ, kCkpt, kB64><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_d(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                     bool capture, bool causal, bool fused_q, cudaStream_t s) {
-    if (capture) return launch_one<D, true, false>(p, tq, tk, tv, s);
-    if (fused_q)
-        return causal ? launch_one<D, false, true, true>(p, tq, tk, tv, s)
-                      : launch_one<D, false, false, true>(p, tq, tk, tv, s);
-    return causal ? launch_one<D, false, true>(p, tq, tk, tv, s) : launch_one<D, false, false>(p, tq, tk, tv, s);
+                     const AttnMode& m, cudaStream_t s) {
+    if (m.capture) return launch_one<D, true, false>(p, tq, tk, tv, s);   // S does not depend on BKV
+    if (m.bkv64) {
+        if (m.fused_q) return cudaErrorInvalidValue;
+        return m.causal ? launch_one<D, false, true, false, false, true>(p, tq, tk, tv, s)
+                        : launch_one<D, false, false, false, false, true>(p, tq, tk, tv, s);
+    }
+    if (m.fused_q)
+        return m.causal ? launch_one<D, false, true, true>(p, tq, tk, tv, s)
+                        : launch_one<D, false, false, true>(p, tq, tk, tv, s);
+    return m.causal ? launch_one<D, false, true>(p, tq, tk, tv, s) : launch_one<D, false, false>(p, tq, tk, tv, s);
 }
 
 }  // namespace
 
 cudaError_t launch_attn(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                        const CUtensorMap& tv, bool capture, bool causal, bool fused_q, cudaStream_t s,
-                        int* launches) {
+                        const CUtensorMap& tv, const AttnMode& mode, cudaStream_t s, int* launches) {
     *launches = 1;
-    if (p.D == 128) return launch_d<128>(p, tq, tk, tv, capture, causal, fused_q, s);
-    if (p.D == 64) return launch_d<64>(p, tq, tk, tv, capture, causal, fused_q, s);
+    if (p.D == 128) return launch_d<128>(p, tq, tk, tv, mode, s);
+    if (p.D == 64) return launch_d<64>(p, tq, tk, tv, mode, s);
     return cudaErrorInvalidValue;
 }
 

@@ -41,6 +41,7 @@ struct PrepParams {
     float* psum;                           // workspace [B,H,n_chunks,D]
     float* pamax;                          // workspace [B,H,n_chunks,D]
     float* v_inv;                          // workspace [B,H,D]
+    float sv;                              // target |v| of the V codes: 144 / BKV (1.125 or 2.25)
 };
 
 // Stage checkpoints of one query tile (see sage_attn_checkpoints).
@@ -81,10 +82,15 @@ int* device_status_ptr();                  // per-device address of the status w
 // with_q = false: K/V statistics and quantization only (Q is quantized by the
 // attention kernel of the fused entry point).
 cudaError_t launch_prep(const PrepParams& p, bool with_q, cudaStream_t s, int* launches);
-// fused_q: tq maps BF16 Q and each CTA quantizes its own Q block.
+// Which form of the attention kernel to launch.
+struct AttnMode {
+    bool capture = false;   // QK checkpoint only (int32 scores)
+    bool causal = false;    // causal mask
+    bool fused_q = false;   // tq maps BF16 Q and each CTA quantizes its own Q block
+    bool bkv64 = false;     // BKV = 64 contract: two 64-key softmax/PV epochs per 128-key tile
+};
 cudaError_t launch_attn(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                        const CUtensorMap& tv, bool capture, bool causal, bool fused_q, cudaStream_t s,
-                        int* launches);
+                        const CUtensorMap& tv, const AttnMode& mode, cudaStream_t s, int* launches);
 // One CTA (p.ck.b, p.ck.h, p.ck.qtile) of the attention kernel, writing its
 // stage checkpoints besides its output rows.
 cudaError_t launch_attn_checkpoints(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,

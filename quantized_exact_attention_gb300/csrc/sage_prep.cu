@@ -214,8 +214,8 @@ __global__ void __launch_bounds__(128) prep_finalize_kernel(const PrepParams p) 
     }
     const int64_t o = ((int64_t)b * p.H + h) * D + d;
     p.k_mean[o] = lk > 0 ? __fdiv_rn(total, (float)lk) : 0.f;
-    p.v_scale[o] = amax > 0.f ? __fdiv_rn(amax, kSV) : 0.f;
-    p.v_inv[o] = amax > 0.f ? __fdiv_rn(kSV, amax) : 0.f;
+    p.v_scale[o] = amax > 0.f ? __fdiv_rn(amax, p.sv) : 0.f;
+    p.v_inv[o] = amax > 0.f ? __fdiv_rn(p.sv, amax) : 0.f;
 }
 
 // ---------------------------------------------------------------------------

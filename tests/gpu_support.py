@@ -59,12 +59,12 @@ class GpuRun:
         self.bufs = S.alloc_prep_buffers(w.B, w.H, w.Nq, w.Nkv, "cuda", int8_codes=int8_codes, D=w.D)
         self.out = None
 
-    def prep(self):
-        S.sage_prep_qkv(self.q, self.k, self.v, self.bufs, self.q_len, self.kv_len)
+    def prep(self, bkv=128):
+        S.sage_prep_qkv(self.q, self.k, self.v, self.bufs, self.q_len, self.kv_len, bkv=bkv)
         torch.cuda.synchronize()
         return self
 
-    def attn(self, fill=None, causal=False):
+    def attn(self, fill=None, causal=False, bkv=128):
         w = self.w
         base = torch.empty((w.B, w.Nq, w.H, w.D), dtype=torch.bfloat16, device="cuda")
         if fill is None:
@@ -72,7 +72,7 @@ class GpuRun:
         else:
             base.fill_(fill)
         self.out = base.permute(0, 2, 1, 3)
-        S.sage_attn_fwd(self.bufs, self.out, self.q_len, self.kv_len, Nkv=w.Nkv, causal=causal)
+        S.sage_attn_fwd(self.bufs, self.out, self.q_len, self.kv_len, Nkv=w.Nkv, causal=causal, bkv=bkv)
         torch.cuda.synchronize()
         assert S.sage_get_device_status() == S.SAGE_OK
         return self

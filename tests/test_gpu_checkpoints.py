@@ -4,7 +4,8 @@ FP8 probability, rescale, FP16 PV, FP32 RO and reciprocal).
 
 Each stage is checked where its inputs are pinned:
   m       bit-exact vs the oracle (a maximum of RN(S * f), order-free)
-  alpha   vs the oracle's exact exp2 within ex2.approx error (same argument)
+  alpha   vs the oracle's exact exp2 within ex2.approx error (same argument);
+          below 2^-126 the GPU's flush to zero is accepted
   P8      e4m3 codes adjacent to the oracle's, and rarely different
   PV16    within four FP16 roundings of the exact sum of the GPU's own P bytes
           times the V codes (the tensor core accumulates 4 K-steps in FP16)
@@ -73,9 +74,11 @@ def test_stage_checkpoints(name):
         width = min(128, int(vis.max()) - t * 128)
         # m: bit-exact
         assert np.array_equal(ck["m"][t, rl].view(np.uint32), ref.m[t].view(np.uint32)), f"m tile {t}"
-        # alpha: ex2.approx of the same argument
+        # alpha: ex2.approx of the same argument; the GPU flushes results below
+        # the FP32 normal range (2^-126) to zero where the oracle keeps subnormals
         a_g, a_r = ck["alpha"][t, rl].astype(np.float64), ref.alpha[t].astype(np.float64)
-        assert np.all(np.abs(a_g - a_r) <= 2.0 ** -21 * np.maximum(a_r, 2.0 ** -126)), f"alpha tile {t}"
+        tol = np.where(a_r < 2.0 ** -126, 2.0 ** -126, 2.0 ** -21 * a_r)
+        assert np.all(np.abs(a_g - a_r) <= tol), f"alpha tile {t}"
         # P8: adjacent codes, rare differences; columns beyond the visible keys are 0
         g8 = ck["p8"][t, rl, :width].astype(np.int32)
         r8 = ref.p8[t].astype(np.int32)
