@@ -8,6 +8,8 @@ fused [B, N, 3, H, D] projection buffer, non-causal.  The metric is
 larger than the 129 MB L2, so no L2 flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --forms     # one JSON line per form of the path (not the
+                              # contract line): causal, fused entry, BKV = 64, D = 64
 
 --impl reference times the CPU oracle (the only other implementation of the
 contract; no other implementation exists to install) on a bounded sample of
@@ -45,6 +47,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--forms", action="store_true",
+                    help="time every form of the path on the bench workload shape instead")
     return ap.parse_args()
 
 
@@ -340,9 +344,77 @@ def run_e2e(args, w, phys, o_phys, bufs, stream, world, ops, dev):
             "api": "sage_attention_host (pinned host buffers, copies inside the timed region)"}
 
 
+def run_forms(args):
+    """Step and attention time of each form of the path on the bench workload
+    shape (16K tokens, strided NHD); one JSON line per form.  Step = everything
+    the form needs from BF16 inputs to BF16 output; causal forms count half
+    of the 4*H*N^2*D operations."""
+    import torch
+
+    import quantized_exact_attention_gb300 as S
+    from quantized_exact_attention_gb300 import build as B
+    from quantized_exact_attention_gb300 import workloads as W
+
+    B.build()
+    S.load_library()
+    spec = dict(W.CONFIGS[CONFIG_ID])
+    forms = [("default", 128, False, 128, "two_calls"), ("causal", 128, True, 128, "two_calls"),
+             ("fused_entry", 128, False, 128, "fused"), ("fused_entry_causal", 128, True, 128, "fused"),
+             ("bkv64", 128, False, 64, "two_calls"), ("d64", 64, False, 128, "two_calls"),
+             ("d64_causal", 64, True, 128, "two_calls")]
+    K = max(3, min(args.steps, 20))
+    for name, d, causal, bkv, path in forms:
+        sp = dict(spec, D=d, H=spec["H"] * 128 // d, name=f"{spec['name']}_D{d}")
+        w = W.make_custom(**sp)
+        phys = w.to("cuda")
+        q, k, v = w.views(phys)
+        bufs = S.alloc_prep_buffers(w.B, w.H, w.Nq, w.Nkv, "cuda", D=d)
+        o = torch.empty((w.B, w.Nq, w.H, d), dtype=torch.bfloat16, device="cuda").permute(0, 2, 1, 3)
+
+        def step():
+            if path == "fused":
+                S.sage_attention(q, k, v, o, bufs, causal=causal)
+            else:
+                S.sage_prep_qkv(q, k, v, bufs, bkv=bkv)
+                S.sage_attn_fwd(bufs, o, causal=causal, bkv=bkv)
+
+        for _ in range(max(args.warmup, 3)):
+            step()
+        torch.cuda.synchronize()
+        steps, attn = [], []
+        for _ in range(K):
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            e[0].record()
+            step()
+            e[1].record()
+            if path != "fused":
+                S.sage_attn_fwd(bufs, o, causal=causal, bkv=bkv)
+            e[2].record()
+            torch.cuda.synchronize()
+            steps.append(e[0].elapsed_time(e[1]))
+            if path != "fused":
+                attn.append(e[1].elapsed_time(e[2]))
+        if S.sage_get_device_status() != S.SAGE_OK:
+            raise RuntimeError(f"device status reports an error in form {name}")
+        ops = w.ops() * (0.5 if causal else 1.0)
+        st = statistics.median(steps)
+        line = {"form": name, "D": d, "H": w.H, "N": w.Nq, "causal": causal, "bkv": bkv, "entry": path,
+                "step_ms_p50": st, "step_tops": ops / st / 1e9, "steps": K}
+        if attn:
+            at = statistics.median(attn)
+            line.update(attn_ms_p50=at, attn_tops=ops / at / 1e9)
+        print(json.dumps(line), flush=True)
+        del phys, q, k, v, bufs, o
+        torch.cuda.empty_cache()
+
+
 def main():
     args = parse_args()
     world, rank, local = dist_env()
+    if args.forms:
+        if rank == 0:
+            run_forms(args)
+        return
     if args.impl == "reference":
         run_reference(args, world, rank)
         return
