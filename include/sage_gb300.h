@@ -233,6 +233,16 @@ int sage_attention_host(const sage_copy* inputs, int n_inputs,
                         const sage_copy* output,
                         int B, int H, int Nq, int Nkv, int D, float sm_scale, void* stream);
 
+/* Launch form of sage_attn_fwd and sage_attn_fwd_causal (process-wide;
+ * returns the previous setting).  1: adjacent query tiles run as clusters of
+ * two CTAs sharing each tensor-core instruction (tcgen05 .cta_group::2, 256
+ * rows), each CTA loading half of every K and V tile.  0 (default): one CTA
+ * per 128-row query tile.  Both forms compute the same values in the same
+ * order (bit-identical outputs); the other entry points always use the
+ * one-CTA form.  On GB300 the paired form is slower for this kernel: every
+ * tile's PV waits for P-ready arrivals from both CTAs, which cross SMs. */
+int sage_set_cta_pairing(int enable);
+
 /* Synchronizes the device, returns the first error a kernel recorded since
  * the last call (SAGE_OK if none) and clears it. */
 int sage_get_device_status(void);

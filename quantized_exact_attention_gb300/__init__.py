@@ -30,7 +30,8 @@ HEAD_DIMS = (64, 128)       # head dimensions the kernels are built for
 
 # Names the header declares (checked by the CPU tests against the .so exports).
 EXPORTED = ("sage_buffer_sizes", "sage_prep_qkv", "sage_attn_fwd", "sage_attn_fwd_causal", "sage_attention",
-            "sage_attn_checkpoints", "sage_prep_qkv_bkv", "sage_attn_fwd_bkv", "sage_qk_int32",
+            "sage_attn_checkpoints", "sage_prep_qkv_bkv", "sage_attn_fwd_bkv", "sage_set_cta_pairing",
+            "sage_qk_int32",
             "sage_attention_host", "sage_get_device_status", "sage_status_string",
             "sage_last_launch_count", "sage_debug_inject_fault", "sage_prep_qkv_noalloc",
             "sage_prep_noalloc_capacity")
@@ -103,6 +104,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sage_status_string.restype = ctypes.c_char_p
     lib.sage_last_launch_count.argtypes = []
     lib.sage_debug_inject_fault.argtypes = [i]
+    lib.sage_set_cta_pairing.argtypes = [i]
     lib.sage_prep_qkv_noalloc.argtypes = lib.sage_prep_qkv.argtypes
     lib.sage_prep_noalloc_capacity.argtypes = []
     for name in EXPORTED:
@@ -312,6 +314,11 @@ def sage_get_device_status() -> int:
 
 def sage_last_launch_count() -> int:
     return int(load_library().sage_last_launch_count())
+
+
+def sage_set_cta_pairing(enable: bool) -> bool:
+    """Select the CTA-pair form of sage_attn_fwd[_causal]; returns the previous setting."""
+    return bool(load_library().sage_set_cta_pairing(1 if enable else 0))
 
 
 def sage_debug_inject_fault(mode: int):

@@ -105,6 +105,7 @@ int check_prep_buffers(const sage_prep_buffers* p, bool need_workspace, const sa
 int status_from(cudaError_t e) { return e == cudaSuccess ? SAGE_OK : SAGE_ERR_LAUNCH; }
 
 int fault_mode_for_next_launch = 0;
+int g_cta_pairing = 0;          // sage_set_cta_pairing (pairs measured slower; off by default)
 
 }  // namespace
 
@@ -221,16 +222,19 @@ static int attn_common(const sage_prep_buffers* in, const sage_tensor* o, int32_
     if (status == nullptr) return SAGE_ERR_LAUNCH;
 
     const uint64_t bh = (uint64_t)B * H;
+    // CTA pairs serve the default and causal forms; each CTA of a pair loads
+    // half of every K tile (64 keys) and of every V tile (D/2 channels)
+    const bool pair = g_cta_pairing != 0 && !capture && ck == nullptr && !bkv64;
     CUtensorMap tq, tk, tv;
     // Q/K code images: boxes of 64 channels (128 bytes, one swizzle row) x 128
-    // rows; V^T: boxes of 128 tokens x D channels.
+    // rows (K: 64 rows when paired); V^T: boxes of 128 tokens x D (D/2) channels.
     const uint64_t d = (uint64_t)D;
     if (!encode_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, in->q16, d, (uint64_t)Nq, bh, d * 2,
                    (uint64_t)Nq * d * 2, 64, 128) ||
         !encode_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, in->k16, d, (uint64_t)Nkv, bh, d * 2,
-                   (uint64_t)Nkv * d * 2, 64, 128) ||
+                   (uint64_t)Nkv * d * 2, 64, pair ? 64 : 128) ||
         !encode_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, in->v8t, (uint64_t)sz.nkv_pad, d, bh,
-                   (uint64_t)sz.nkv_pad, (uint64_t)sz.nkv_pad * d, 128, (uint32_t)D))
+                   (uint64_t)sz.nkv_pad, (uint64_t)sz.nkv_pad * d, 128, (uint32_t)(pair ? D / 2 : D)))
         return encode_fn() ? SAGE_ERR_UNSUPPORTED : SAGE_ERR_DRIVER;
 
     AttnParams p{};
@@ -259,6 +263,7 @@ static int attn_common(const sage_prep_buffers* in, const sage_tensor* o, int32_
         mode.capture = capture;
         mode.causal = causal;
         mode.bkv64 = bkv64;
+        mode.pair = pair;
         rc = status_from(launch_attn(p, tq, tk, tv, mode, static_cast<cudaStream_t>(stream), &launches));
     }
     if (rc == SAGE_OK) g_last_launches = launches;
@@ -434,6 +439,12 @@ const char* sage_status_string(int code) {
 }
 
 int sage_last_launch_count(void) { return g_last_launches; }
+
+int sage_set_cta_pairing(int enable) {
+    const int old = g_cta_pairing;
+    g_cta_pairing = enable != 0;
+    return old;
+}
 
 // Test hook (not part of the public header): the next sage_attn_fwd launch
 // withholds one V tile copy so its consumer's bounded wait runs out.

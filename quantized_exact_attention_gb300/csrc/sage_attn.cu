@@ -78,12 +78,16 @@ enum Bar : uint32_t {
 // Shared-memory map for head dimension D (offsets from a 1024-byte aligned
 // base).  Q and K tiles hold 128 rows of FP16 codes as D/64 column blocks of
 // kHalfBytes; a V tile holds D channel rows of 128 e4m3 tokens.
-template <int D>
+// Paired CTAs (kPair) hold only their half of each K tile (64 keys) and of
+// each V tile (D/2 channels).
+template <int D, bool kPair = false>
 struct Smem {
     static_assert(D == 64 || D == 128, "head dimension");
     static constexpr uint32_t kTileQBytes = 128 * D * 2;
-    static constexpr uint32_t kTileKBytes = 128 * D * 2;
-    static constexpr uint32_t kTileVBytes = 128 * D;
+    static constexpr uint32_t kKRows = kPair ? 64 : 128;        // keys of a K stage
+    static constexpr uint32_t kKBlock = kKRows * 128;          // one 64-channel column block of a K stage
+    static constexpr uint32_t kTileKBytes = kKRows * D * 2;
+    static constexpr uint32_t kTileVBytes = 128 * (kPair ? D / 2 : D);
     static constexpr uint32_t OFF_Q = 0;
     static constexpr uint32_t OFF_K = OFF_Q + kTileQBytes;
     static constexpr uint32_t OFF_V = OFF_K + kNK * kTileKBytes;
@@ -126,11 +130,6 @@ __device__ __forceinline__ void record_failure(const AttnParams& p, volatile int
     }
 }
 
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
-    const bool ok = mbar_wait(bar, parity, abort_flag);
-    return __all_sync(0xffffffffu, ok);
-}
-
 __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
     const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
     const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
@@ -150,11 +149,21 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
 // epochs: keys 0-63 (half 0) then keys 64-127 (half 1), each with its own
 // running maximum, rescale and FP16 PV sum (two PV groups of K = 64 through
 // the one PV accumulator) and its own RO update.
-template <int D, bool kCapture, bool kCausal, bool kFusedQ, bool kCkpt = false, bool kB64 = false>
+// kPair: a cluster of two CTAs computes two adjacent query tiles of one head
+// with shared MMAs (tcgen05 .cta_group::2, M = 256).  Rank 0 issues every MMA
+// for both; each CTA loads its own Q tile, one half of every K tile (64 keys)
+// and one half of every V tile (D/2 channels), and holds its own S, P, PV,
+// softmax and correction state.  Loads of both CTAs complete on rank 0's
+// barriers; rank 0's commits arrive on both CTAs' barriers; the P-ready and
+// PV-consumed arrivals of both CTAs' warps go to rank 0.
+template <int D, bool kCapture, bool kCausal, bool kFusedQ, bool kCkpt = false, bool kB64 = false,
+          bool kPair = false>
 __global__ void __launch_bounds__(kThreads, 1)
 sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
-    using L = Smem<D>;
+    static_assert(!kPair || (!kCapture && !kFusedQ && !kCkpt && !kB64), "paired CTAs: default and causal forms");
+    using L = Smem<D, kPair>;
+    constexpr uint32_t kKBlock = L::kKBlock;
     constexpr uint32_t kTileQBytes = L::kTileQBytes, kTileKBytes = L::kTileKBytes, kTileVBytes = L::kTileVBytes;
     constexpr uint32_t OFF_Q = L::OFF_Q, OFF_K = L::OFF_K, OFF_V = L::OFF_V, OFF_BAR = L::OFF_BAR;
     constexpr uint32_t OFF_ALPHA = L::OFF_ALPHA, OFF_XM = L::OFF_XM, OFF_L = L::OFF_L, OFF_VS = L::OFF_VS;
@@ -167,17 +176,29 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // causal: the longest query tiles start first
-    const int qtile = kCkpt ? p.ck.qtile : (kCausal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x);
+    uint32_t rank = 0;                                      // kPair: rank in the CTA pair
+    int qtile;
+    if constexpr (kPair) {
+        rank = cluster_ctarank();
+        const int npairs = (int)(gridDim.x >> 1);
+        const int pi = kCausal ? npairs - 1 - (int)(blockIdx.x >> 1) : (int)(blockIdx.x >> 1);
+        qtile = 2 * pi + (int)rank;
+    } else {
+        // causal: the longest query tiles start first
+        qtile = kCkpt ? p.ck.qtile : (kCausal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x);
+    }
     const int h = kCkpt ? p.ck.h : (int)blockIdx.y, b = kCkpt ? p.ck.b : (int)blockIdx.z;
     const int bh = b * p.H + h;
     const int q0 = qtile * 128;
     const int lq = clamp_len(p.q_len, b, p.Nq);
     const int lk = clamp_len(p.kv_len, b, p.Nkv);
-    if (q0 >= lq) return;                                   // no valid row in this tile
+    // a pair takes every decision below from its first tile so both CTAs agree
+    const int qg0 = kPair ? (qtile & ~1) * 128 : q0;        // first row of the CTA group
+    constexpr int kGroupRows = kPair ? 256 : 128;
+    if (qg0 >= lq) return;                                  // no valid row in this CTA group
     const int diag = lk - lq;                               // causal: row i sees keys j <= i + diag
-    // keys any row of this tile can see
-    const int kv_end = kCausal ? min(lk, min(q0 + 127, lq - 1) + diag + 1) : lk;
+    // keys any row of this CTA group can see
+    const int kv_end = kCausal ? min(lk, min(qg0 + kGroupRows - 1, lq - 1) + diag + 1) : lk;
 
     if (kv_end <= 0) {                                      // no keys: rows are zero
         if (!kCapture && threadIdx.x < 128) {
@@ -198,6 +219,23 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     float* vs_s = reinterpret_cast<float*>(sgen + OFF_VS);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sgen + OFF_TMEM);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + OFF_ABORT);
+    const uint32_t peer_abort = kPair ? mapa_rank(sbase + OFF_ABORT, rank ^ 1u) : 0u;
+    // waits, commits and failure reports of this kernel form
+    auto bwait = [&](uint32_t bb, uint32_t par, const volatile int* af) -> bool {
+        if constexpr (kPair) return mbar_wait_cluster(bb, par, af);
+        else return mbar_wait(bb, par, af);
+    };
+    auto wwait = [&](uint32_t bb, uint32_t par, const volatile int* af) -> bool {
+        return __all_sync(0xffffffffu, bwait(bb, par, af));
+    };
+    auto commit = [&](uint32_t bb) {
+        if constexpr (kPair) mma_commit2(bb);
+        else mma_commit(bb);
+    };
+    auto fail = [&](int role, int tile) {
+        record_failure(p, abort_flag, role, tile);
+        if constexpr (kPair) st_cluster_u32(peer_abort, 1u);  // the peer leaves its loops too
+    };
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
@@ -207,10 +245,10 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         for (int i = 0; i < kNS; ++i) {
             mbar_init(bar(B_SFULL + i), 1);
             mbar_init(bar(B_SFREE + i), 256);     // every softmax thread
-            mbar_init(bar(B_PFULL + i), 256);     // every softmax thread
+            mbar_init(bar(B_PFULL + i), kPair ? 16 : 256);   // every softmax thread / warp of both CTAs
         }
         mbar_init(bar(B_PVFULL), 1);
-        mbar_init(bar(B_PVFREE), 256);            // every correction thread
+        mbar_init(bar(B_PVFREE), kPair ? 16 : 256);       // every correction thread / warp of both CTAs
         for (int i = 0; i < 8; ++i) mbar_init(bar(B_XM + i), 64);    // both halves of 32 rows
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B_AFULL + i), 128);     // softmax half 0 (writes alpha)
@@ -222,8 +260,13 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         fence_mbar_init();
     }
     if (warp == kWarpMma) {
-        tmem_alloc(sbase + OFF_TMEM, kTmemCols);
-        tmem_relinquish();
+        if constexpr (kPair) {
+            tmem_alloc2(sbase + OFF_TMEM, kTmemCols);
+            tmem_relinquish2();
+        } else {
+            tmem_alloc(sbase + OFF_TMEM, kTmemCols);
+            tmem_relinquish();
+        }
     }
     if (warp == kWarpProducer && lane == 0) {
         tma_prefetch_desc(&tm_q);
@@ -232,6 +275,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (kPair) cluster_sync_all();               // the peer's barriers exist before remote traffic
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
@@ -245,8 +289,8 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // chunk's row is its byte offset / 128 within its 64-channel block.
             const int ct = threadIdx.x;                     // 0..511
             constexpr int kChunks = (int)(kTileQBytes / 16 / 512);
-            const bool got = warp_wait(bar(B_QFULL), 0, abort_flag);
-            if (!got && lane == 0) record_failure(p, abort_flag, R_SOFTMAX, -1);
+            const bool got = wwait(bar(B_QFULL), 0, abort_flag);
+            if (!got && lane == 0) fail(R_SOFTMAX, -1);
             uint4 xq[kChunks];
             float amax = 0.f;
 #pragma unroll
@@ -303,8 +347,8 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const int kb_next = 2 * (t + 1) + half;
             ks_next = (kb_next * 64 < lk) ? kscale[kb_next] : 0.f;
             const float f = __fmul_rn(__fmul_rn(qs, ks), p.c);
-            if (!warp_wait(bar(B_SFULL + s3), s3ph, abort_flag)) {
-                if (lane == 0) record_failure(p, abort_flag, R_SOFTMAX, t);
+            if (!wwait(bar(B_SFULL + s3), s3ph, abort_flag)) {
+                if (lane == 0) fail(R_SOFTMAX, t);
                 ok = false;
                 break;
             }
@@ -360,8 +404,8 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // values (tcgen05.wait::ld + fence before the s_free arrival), so
             // after this barrier either half may overwrite S columns with P.
             mbar_arrive(bar(B_XM + sb * 4 + quarter));
-            if (!warp_wait(bar(B_XM + sb * 4 + quarter), (t >> 1) & 1, abort_flag)) {
-                if (lane == 0) record_failure(p, abort_flag, R_SOFTMAX, t);
+            if (!wwait(bar(B_XM + sb * 4 + quarter), (t >> 1) & 1, abort_flag)) {
+                if (lane == 0) fail(R_SOFTMAX, t);
                 ok = false;
                 break;
             }
@@ -423,8 +467,8 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
             tmem_wait_st();
             if (half == 0) {
-                if (t >= 2 && !warp_wait(bar(B_AFREE + sb), ((t >> 1) - 1) & 1, abort_flag)) {
-                    if (lane == 0) record_failure(p, abort_flag, R_SOFTMAX, t);
+                if (t >= 2 && !wwait(bar(B_AFREE + sb), ((t >> 1) - 1) & 1, abort_flag)) {
+                    if (lane == 0) fail(R_SOFTMAX, t);
                     ok = false;
                     break;
                 }
@@ -432,7 +476,12 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (kB64) alpha_s[(sb * 2 + 1) * 128 + row] = alpha_b;
             }
             tc_fence_before();
-            mbar_arrive(bar(B_PFULL + s3));
+            if constexpr (kPair) {                          // one arrival per warp, on rank 0's barrier
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(mapa_rank(bar(B_PFULL + s3), 0));
+            } else {
+                mbar_arrive(bar(B_PFULL + s3));
+            }
             if (half == 0) mbar_arrive(bar(B_AFULL + sb));
             if constexpr (kB64) {
                 // half 0's keys join in epoch A, half 1's in epoch B
@@ -462,8 +511,8 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             bool ok = true;
             for (int t = 0; t < T; ++t) {
                 const int sb = t & 1;
-                if (!warp_wait(bar(B_AFULL + sb), (t >> 1) & 1, abort_flag)) {
-                    if (lane == 0) record_failure(p, abort_flag, R_CORRECT, t);
+                if (!wwait(bar(B_AFULL + sb), (t >> 1) & 1, abort_flag)) {
+                    if (lane == 0) fail(R_CORRECT, t);
                     ok = false;
                     break;
                 }
@@ -474,8 +523,8 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 for (int e = 0; e < (kB64 ? 2 : 1); ++e) {  // PV epochs of this tile
                     const float alpha = e ? alpha_b : alpha_a;
                     const bool unit = __all_sync(0xffffffffu, alpha == 1.0f);   // RN(RO * 1) == RO
-                    if (!warp_wait(bar(B_PVFULL), kB64 ? e : (t & 1), abort_flag)) {
-                        if (lane == 0) record_failure(p, abort_flag, R_CORRECT, t);
+                    if (!wwait(bar(B_PVFULL), kB64 ? e : (t & 1), abort_flag)) {
+                        if (lane == 0) fail(R_CORRECT, t);
                         ok = false;
                         break;
                     }
@@ -487,7 +536,12 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         tmem_wait_ld();
                         if (c == kDH / 32 - 1) {
                             tc_fence_before();
-                            mbar_arrive(bar(B_PVFREE));
+                            if constexpr (kPair) {          // one arrival per warp, on rank 0's barrier
+                                __syncwarp();
+                                if (lane == 0) mbar_arrive_cluster(mapa_rank(bar(B_PVFREE), 0));
+                            } else {
+                                mbar_arrive(bar(B_PVFREE));
+                            }
                         }
                         if constexpr (kCkpt) {
                             uint4* dp = reinterpret_cast<uint4*>(p.ck.pv16 + ((int64_t)t * 128 + row) * D + half * kDH +
@@ -512,7 +566,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     for (int i = 0; i < kDH / 4; ++i) dp[i] = make_float4(ro[4 * i], ro[4 * i + 1], ro[4 * i + 2], ro[4 * i + 3]);
                 }
             }
-            if (ok && warp_wait(bar(B_LFULL), 0, abort_flag)) {
+            if (ok && wwait(bar(B_LFULL), 0, abort_flag)) {
                 // l carries the 448 scale of P, so (RO / l) * v_scale is the output
                 const float l_row = l_s[row] + l_s[128 + row];
                 // causal rows that saw no key have l = 0 and RO = 0: write zeros
@@ -537,7 +591,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     }
                 }
             } else if (ok) {
-                if (lane == 0) record_failure(p, abort_flag, R_CORRECT, T);
+                if (lane == 0) fail(R_CORRECT, T);
             }
         }
     } else if (warp == kWarpProducer) {
@@ -548,31 +602,46 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             for (int i = 0; i < kNK; ++i) last_k[i] = -1;
             for (int i = 0; i < kNV; ++i) last_v[i] = -1;
             bool ok = true;
-            mbar_arrive_expect_tx(bar(B_QFULL), kTileQBytes);
+            // kPair: rank 0 expects the bytes of both CTAs; both complete on rank 0's barrier
+            const uint32_t qfull = kPair ? mapa_rank(bar(B_QFULL), 0) : bar(B_QFULL);
+            if (rank == 0) mbar_arrive_expect_tx(bar(B_QFULL), (kPair ? 2 : 1) * kTileQBytes);
 #pragma unroll
             for (int hh = 0; hh < D / 64; ++hh) {
                 if constexpr (kFusedQ)
                     tma_load_4d(sQ + hh * kHalfBytes, &tm_q, hh * 64, q0, h, b, bar(B_QFULL));
+                else if constexpr (kPair)
+                    tma_load_3d_pair(sQ + hh * kHalfBytes, &tm_q, hh * 64, q0, bh, qfull);
                 else
                     tma_load_3d(sQ + hh * kHalfBytes, &tm_q, hh * 64, q0, bh, bar(B_QFULL));
             }
             auto load_k = [&](int t) -> bool {
                 const int st = t % kNK;
-                if (t >= kNK && !mbar_wait(bar(B_KEMPTY + st), ((t / kNK) - 1) & 1, abort_flag)) return false;
+                if (t >= kNK && !bwait(bar(B_KEMPTY + st), ((t / kNK) - 1) & 1, abort_flag)) return false;
                 const uint32_t dst = sbase + OFF_K + st * kTileKBytes;
-                mbar_arrive_expect_tx(bar(B_KFULL + st), kTileKBytes);
+                if (rank == 0) mbar_arrive_expect_tx(bar(B_KFULL + st), (kPair ? 2 : 1) * kTileKBytes);
 #pragma unroll
-                for (int hh = 0; hh < D / 64; ++hh)
-                    tma_load_3d(dst + hh * kHalfBytes, &tm_k, hh * 64, t * 128, bh, bar(B_KFULL + st));
+                for (int hh = 0; hh < D / 64; ++hh) {
+                    if constexpr (kPair)                    // keys [t*128 + 64*rank, +64)
+                        tma_load_3d_pair(dst + hh * kKBlock, &tm_k, hh * 64, t * 128 + 64 * (int)rank, bh,
+                                         mapa_rank(bar(B_KFULL + st), 0));
+                    else
+                        tma_load_3d(dst + hh * kHalfBytes, &tm_k, hh * 64, t * 128, bh, bar(B_KFULL + st));
+                }
                 last_k[st] = t;
                 return true;
             };
             auto load_v = [&](int t) -> bool {
                 const int st = t % kNV;
-                if (t >= kNV && !mbar_wait(bar(B_VEMPTY + st), ((t / kNV) - 1) & 1, abort_flag)) return false;
+                if (t >= kNV && !bwait(bar(B_VEMPTY + st), ((t / kNV) - 1) & 1, abort_flag)) return false;
                 const uint32_t dst = sbase + OFF_V + st * kTileVBytes;
-                mbar_arrive_expect_tx(bar(B_VFULL + st), kTileVBytes);
-                if (p.fault_mode != 1) tma_load_3d(dst, &tm_v, t * 128, 0, bh, bar(B_VFULL + st));
+                if (rank == 0) mbar_arrive_expect_tx(bar(B_VFULL + st), (kPair ? 2 : 1) * kTileVBytes);
+                if (p.fault_mode != 1) {
+                    if constexpr (kPair)                    // channels [rank*D/2, +D/2)
+                        tma_load_3d_pair(dst, &tm_v, t * 128, (int)rank * (D / 2), bh,
+                                         mapa_rank(bar(B_VFULL + st), 0));
+                    else
+                        tma_load_3d(dst, &tm_v, t * 128, 0, bh, bar(B_VFULL + st));
+                }
                 last_v[st] = t;
                 return true;
             };
@@ -580,29 +649,34 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // K(t+2), V(t) for every tile t.
             ok = load_k(0);
             if (ok && T > 1) ok = load_k(1);
-            if (!ok) record_failure(p, abort_flag, R_PRODUCER, 0);
+            if (!ok) fail(R_PRODUCER, 0);
             for (int t = 0; t < T && ok; ++t) {
                 if (t + 2 < T) ok = load_k(t + 2);
                 if (ok && !kCapture) ok = load_v(t);
-                if (!ok) record_failure(p, abort_flag, R_PRODUCER, t);
+                if (!ok) fail(R_PRODUCER, t);
             }
-            // Drain: every copy issued must land before the CTA may exit.
+            // Drain: every copy issued must land before the CTA may exit.  A pair's
+            // copies complete on rank 0's barriers: rank 0 drains for both, and
+            // the closing cluster barrier keeps rank 1 alive until then.
             const int zero = 0;
             const volatile int* no_abort = &zero;
-            mbar_wait(bar(B_QFULL), 0, no_abort);
-            for (int i = 0; i < kNK; ++i)
-                if (last_k[i] >= 0) mbar_wait(bar(B_KFULL + i), (last_k[i] / kNK) & 1, no_abort);
-            if (p.fault_mode != 1)
-                for (int i = 0; i < kNV; ++i)
-                    if (last_v[i] >= 0) mbar_wait(bar(B_VFULL + i), (last_v[i] / kNV) & 1, no_abort);
+            if (rank == 0) {
+                bwait(bar(B_QFULL), 0, no_abort);
+                for (int i = 0; i < kNK; ++i)
+                    if (last_k[i] >= 0) bwait(bar(B_KFULL + i), (last_k[i] / kNK) & 1, no_abort);
+                if (p.fault_mode != 1)
+                    for (int i = 0; i < kNV; ++i)
+                        if (last_v[i] >= 0) bwait(bar(B_VFULL + i), (last_v[i] / kNV) & 1, no_abort);
+            }
         }
     } else {
         // ===================================================== MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t kIdescQK = idesc_f32acc(0u, 128u, 128u);   // F16 x F16 -> F32
-            constexpr uint32_t kIdescPV = idesc_f16acc(0u, 128u, (uint32_t)D);   // E4M3 x E4M3 -> F16
+        if (lane == 0 && rank == 0) {
+            constexpr uint32_t kM = kPair ? 256u : 128u;                  // rows of both CTAs of a pair
+            constexpr uint32_t kIdescQK = idesc_f32acc(0u, kM, 128u);     // F16 x F16 -> F32
+            constexpr uint32_t kIdescPV = idesc_f16acc(0u, kM, (uint32_t)D);   // E4M3 x E4M3 -> F16
             const uint32_t sQ = sbase + OFF_Q;
-            bool ok = mbar_wait(bar(kFusedQ ? B_QREADY : B_QFULL), 0, abort_flag);
+            bool ok = bwait(bar(kFusedQ ? B_QREADY : B_QFULL), 0, abort_flag);
             int fail_tile = 0;
             // Shared-memory descriptors are built once.  Their start-address field
             // holds (address >> 4) in the low 14 bits; every operand lies below
@@ -617,18 +691,22 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // reuses the buffer of tile t-1, whose S the softmax has read and
             // whose P the PV MMA issued before it (same thread, in order) reads.
             auto issue_qk = [&](int t) -> bool {
-                if (!mbar_wait(bar(B_KFULL + k_st), k_ph, abort_flag)) return false;
-                if (t >= kNS && !mbar_wait(bar(B_SFREE + qb), qph ^ 1, abort_flag)) return false;
+                if (!bwait(bar(B_KFULL + k_st), k_ph, abort_flag)) return false;
+                if (t >= kNS && !bwait(bar(B_SFREE + qb), qph ^ 1, abort_flag)) return false;
                 tc_fence_after();
                 const uint64_t bK = dK + (uint64_t)(k_st * (kTileKBytes >> 4));
                 const uint32_t dS = tmem + TM_S + qb * 128;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
-                    mma_f16_ss(dS, dQ + off, bK + off, kIdescQK, kk > 0 ? 1u : 0u);
+                    const uint32_t off_a = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+                    const uint32_t off_b = ((kk >> 2) * kKBlock + (kk & 3) * 32) >> 4;
+                    if constexpr (kPair)
+                        mma2_f16_ss(dS, dQ + off_a, bK + off_b, kIdescQK, kk > 0 ? 1u : 0u);
+                    else
+                        mma_f16_ss(dS, dQ + off_a, bK + off_b, kIdescQK, kk > 0 ? 1u : 0u);
                 }
-                mma_commit(bar(B_SFULL + qb));
-                mma_commit(bar(B_KEMPTY + k_st));
+                commit(bar(B_SFULL + qb));
+                commit(bar(B_KEMPTY + k_st));
                 if (++k_st == kNK) { k_st = 0; k_ph ^= 1; }
                 if (++qb == kNS) { qb = 0; qph ^= 1; }
                 return true;
@@ -636,25 +714,29 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // The operands that are almost always ready are checked first, so
             // that only the wait for P sits between the softmax and the PV MMA.
             auto issue_pv = [&](int t) -> bool {
-                if (!mbar_wait(bar(B_VFULL + v_st), v_ph, abort_flag)) return false;
+                if (!bwait(bar(B_VFULL + v_st), v_ph, abort_flag)) return false;
                 const uint64_t bV = dV + (uint64_t)(v_st * (kTileVBytes >> 4));
                 const uint32_t aP = tmem + TM_S + pb * 128;
                 constexpr int kEpochs = kB64 ? 2 : 1, kSteps = 4 / kEpochs;   // K = 32 steps per epoch
 #pragma unroll
                 for (int e = 0; e < kEpochs; ++e) {
                     const int n = t * kEpochs + e;                           // PV accumulator use
-                    if (n >= 1 && !mbar_wait(bar(B_PVFREE), (n - 1) & 1, abort_flag)) return false;
-                    if (e == 0 && !mbar_wait(bar(B_PFULL + pb), pph, abort_flag)) return false;
+                    if (n >= 1 && !bwait(bar(B_PVFREE), (n - 1) & 1, abort_flag)) return false;
+                    if (e == 0 && !bwait(bar(B_PFULL + pb), pph, abort_flag)) return false;
                     tc_fence_after();
 #pragma unroll
                     for (int j = 0; j < kSteps; ++j) {
                         const int kk = e * kSteps + j;
-                        mma_f8_ts(tmem + TM_PV, aP + kk * 8, bV + (uint64_t)(kk * (32 >> 4)), kIdescPV,
-                                  j > 0 ? 1u : 0u);
+                        if constexpr (kPair)
+                            mma2_f8_ts(tmem + TM_PV, aP + kk * 8, bV + (uint64_t)(kk * (32 >> 4)), kIdescPV,
+                                       j > 0 ? 1u : 0u);
+                        else
+                            mma_f8_ts(tmem + TM_PV, aP + kk * 8, bV + (uint64_t)(kk * (32 >> 4)), kIdescPV,
+                                      j > 0 ? 1u : 0u);
                     }
-                    mma_commit(bar(B_PVFULL));
+                    commit(bar(B_PVFULL));
                 }
-                mma_commit(bar(B_VEMPTY + v_st));
+                commit(bar(B_VEMPTY + v_st));
                 if (++v_st == kNV) { v_st = 0; v_ph ^= 1; }
                 if (++pb == kNS) { pb = 0; pph ^= 1; }
                 return true;
@@ -666,20 +748,27 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (t + 2 < T) ok = issue_qk(t + 2);
                 if (ok && !kCapture) ok = issue_pv(t);
             }
-            if (!ok) record_failure(p, abort_flag, R_MMA, fail_tile);
+            if (!ok) fail(R_MMA, fail_tile);
             // Drain: all MMAs issued by this thread complete before teardown.
-            mma_commit(bar(B_DRAIN));
+            commit(bar(B_DRAIN));
             const int zero = 0;
-            mbar_wait(bar(B_DRAIN), 0, &zero);
+            bwait(bar(B_DRAIN), 0, &zero);
+        } else if (kPair && lane == 0) {
+            // rank 1: rank 0's MMAs read this CTA's shared memory and write its
+            // tensor memory; they finish before it frees either
+            const int zero = 0;
+            bwait(bar(B_DRAIN), 0, &zero);
         }
     }
 
     tc_fence_before();
     __syncthreads();
+    if constexpr (kPair) cluster_sync_all();               // no remote traffic past this point
     if (warp == kWarpMma) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        if constexpr (kPair) tmem_dealloc2(tmem, kTmemCols);
+        else tmem_dealloc(tmem, kTmemCols);
     }
 }
 
@@ -702,9 +791,45 @@ cudaError_t launch_one(const AttnParams& p, const CUtensorMap& tq, const CUtenso
     return cudaGetLastError();
 }
 
+// Paired form: clusters of two CTAs over an even number of query tiles.
+template <int D, bool kCausal>
+cudaError_t launch_pair(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                        cudaStream_t s) {
+    static bool attr_set[64] = {};
+    constexpr uint32_t kSmemBytes = Smem<D, true>::kSmemBytes;
+    auto kernel = sage_attn_kernel<D, false, kCausal, false, false, false, true>;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    const unsigned pairs = (unsigned)((p.Nq + 255) / 256);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * pairs, (unsigned)p.H, (unsigned)p.B);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 template <int D>
 cudaError_t launch_d(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      const AttnMode& m, cudaStream_t s) {
+    if (m.pair) {
+        if (m.capture || m.fused_q || m.bkv64) return cudaErrorInvalidValue;
+        return m.causal ? launch_pair<D, true>(p, tq, tk, tv, s) : launch_pair<D, false>(p, tq, tk, tv, s);
+    }
     if (m.capture) return launch_one<D, true, false>(p, tq, tk, tv, s);   // S does not depend on BKV
     if (m.bkv64) {
         if (m.fused_q) return cudaErrorInvalidValue;

@@ -88,6 +88,8 @@ struct AttnMode {
     bool causal = false;    // causal mask
     bool fused_q = false;   // tq maps BF16 Q and each CTA quantizes its own Q block
     bool bkv64 = false;     // BKV = 64 contract: two 64-key softmax/PV epochs per 128-key tile
+    bool pair = false;      // clusters of two CTAs sharing M = 256 MMAs (default and causal forms);
+                            // tk / tv then map half tiles (64 keys; D/2 channels)
 };
 cudaError_t launch_attn(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                         const CUtensorMap& tv, const AttnMode& mode, cudaStream_t s, int* launches);
