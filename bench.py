@@ -361,7 +361,8 @@ def run_forms(args):
     forms = [("default", 128, False, 128, "two_calls"), ("causal", 128, True, 128, "two_calls"),
              ("fused_entry", 128, False, 128, "fused"), ("fused_entry_causal", 128, True, 128, "fused"),
              ("bkv64", 128, False, 64, "two_calls"), ("d64", 64, False, 128, "two_calls"),
-             ("d64_causal", 64, True, 128, "two_calls")]
+             ("d64_causal", 64, True, 128, "two_calls"), ("cta_pairs", 128, False, 128, "pairs"),
+             ("cta_pairs_causal", 128, True, 128, "pairs")]
     K = max(3, min(args.steps, 20))
     for name, d, causal, bkv, path in forms:
         sp = dict(spec, D=d, H=spec["H"] * 128 // d, name=f"{spec['name']}_D{d}")
@@ -370,6 +371,8 @@ def run_forms(args):
         q, k, v = w.views(phys)
         bufs = S.alloc_prep_buffers(w.B, w.H, w.Nq, w.Nkv, "cuda", D=d)
         o = torch.empty((w.B, w.Nq, w.H, d), dtype=torch.bfloat16, device="cuda").permute(0, 2, 1, 3)
+
+        S.sage_set_cta_pairing(path == "pairs")
 
         def step():
             if path == "fused":
@@ -394,6 +397,7 @@ def run_forms(args):
             steps.append(e[0].elapsed_time(e[1]))
             if path != "fused":
                 attn.append(e[1].elapsed_time(e[2]))
+        S.sage_set_cta_pairing(False)
         if S.sage_get_device_status() != S.SAGE_OK:
             raise RuntimeError(f"device status reports an error in form {name}")
         ops = w.ops() * (0.5 if causal else 1.0)
