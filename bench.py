@@ -52,6 +52,23 @@ def parse_args():
     return ap.parse_args()
 
 
+def kernel_traffic():
+    """DRAM bytes per launch of the attention kernel from the committed ncu
+    capture (profiles/sage_attn_kernel_counters.json), or None when the
+    kernel source has changed since the counters were taken."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "sage_attn_kernel_counters.json")) as f:
+            rec = json.load(f)
+        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+    except (OSError, KeyError, ValueError):
+        return None
+    if sha != rec.get("source_sha256"):
+        return None
+    return int(rec["dram_bytes_read"]) + int(rec["dram_bytes_write"])
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -271,7 +288,8 @@ def run_ours(args, world, rank, local):
     p8 = 2.0 * p16
     mixed = 2.0 / (1.0 / p16 + 1.0 / p8)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": mixed, "unit": "TFLOP/s",
-                "frac": achieved / mixed, "traffic": None,
+                "frac": achieved / mixed, "traffic": kernel_traffic(),
+                "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
                 "kernel": "sage_attn_kernel (fused QK/softmax/PV)",
                 "peak_basis": (f"{src} bf16 burst {p16:.1f} TF/s for QK (FP16 codes) and 2x that for "
                                f"e4m3 PV; equal op split -> 4/3 x bf16 = {mixed:.1f}"),
