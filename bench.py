@@ -37,6 +37,7 @@ UNIT = "TOPS"
 CONFIG_ID = 4
 DTYPE = "int8 QK (FP16 integer codes) + e4m3 PV, FP32 accumulate, bf16 in/out"
 FALLBACK_BF16_TFLOPS = 1900.0
+E2E_HEAD_GROUPS = 6     # head ranges of the overlapped host entry (4..8 measured best on this workload)
 
 
 def parse_args():
@@ -329,7 +330,11 @@ def run_ours(args, world, rank, local):
 
 
 def run_e2e(args, w, phys, o_phys, bufs, stream, world, ops, dev):
-    """Same metric through sage_attention_host: pinned host in, device compute, host out."""
+    """Same metric through the public host-memory entry points: pinned host
+    inputs in, device compute, host output out, all inside the timed region.
+    The headline uses sage_attention_host_overlapped (copies of one head range
+    overlap the kernels of the others); sage_attention_host (all copies, then
+    the kernels, then the copy back) is reported beside it."""
     import torch
     import torch.distributed as dist
 
@@ -337,29 +342,44 @@ def run_e2e(args, w, phys, o_phys, bufs, stream, world, ops, dev):
     host_in = [t.cpu().pin_memory() for t in phys]
     host_out = torch.empty(o_phys.shape, dtype=o_phys.dtype).pin_memory()
     o_view = o_phys.permute(0, 2, 1, 3)
+    qh, kh, vh = w.views(host_in)
+    qd, kd, vd = w.views(list(phys))
 
-    def once():
+    def sequential():
         S.sage_attention_host(host_in, list(phys), w.views, bufs, o_view, host_out, stream=stream)
 
-    for _ in range(max(args.warmup, 3)):
-        once()
-    torch.cuda.synchronize()
-    K = max(1, min(args.steps, 20))
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    a.record(stream)
-    for _ in range(K):
-        once()
-    b.record(stream)
-    torch.cuda.synchronize()
-    ms = max_over_ranks(a.elapsed_time(b) / K, world, dev)
+    def overlapped():
+        S.sage_attention_host_overlapped(qh, kh, vh, host_out.permute(0, 2, 1, 3), qd, kd, vd, o_view, bufs,
+                                         head_groups=E2E_HEAD_GROUPS, stream=stream)
+
+    def timed(fn):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        torch.cuda.synchronize()
+        K = max(1, min(args.steps, 20))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(K):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return max_over_ranks(a.elapsed_time(b) / K, world, dev), K
+
+    ms, K = timed(overlapped)
+    ms_seq, _ = timed(sequential)
+    if S.sage_get_device_status() != S.SAGE_OK:
+        raise RuntimeError("device status reports an error after the end-to-end steps")
     h2d = sum(x.numel() * x.element_size() for x in host_in)
     d2h = host_out.numel() * host_out.element_size()
     return {"value": whole_job_tops(ops, world, ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": K,
-            "api": "sage_attention_host (pinned host buffers, copies inside the timed region)"}
+            "api": (f"sage_attention_host_overlapped (pinned host buffers, {E2E_HEAD_GROUPS} head ranges, "
+                    "copies inside the timed region)"),
+            "sequential_entry": {"api": "sage_attention_host", "value": whole_job_tops(ops, world, ms_seq),
+                                 "ms_per_step": ms_seq}}
 
 
 def run_forms(args):

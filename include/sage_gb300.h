@@ -243,6 +243,35 @@ int sage_attention_host(const sage_copy* inputs, int n_inputs,
  * tile's PV waits for P-ready arrivals from both CTAs, which cross SMs. */
 int sage_set_cta_pairing(int enable);
 
+/* End-to-end call from host memory with the copies overlapped with the
+ * compute.  The heads of a problem are independent (K mean, quantization
+ * scales and attention are all per (b, h)), so the call splits the heads into
+ * head_groups contiguous ranges and, for each range on one of three internal
+ * streams, copies its Q/K/V rows host->device, prepares them, runs the
+ * attention and copies its output rows device->host; the copies of one range
+ * overlap the kernels of the others.
+ *  q_host, k_host, v_host, o_host : host (pinned) tensors with the same
+ *            element strides as the device tensors q, k, v, o ([B,H,N,D]
+ *            views, BF16); only the logical elements are copied, one 2-D
+ *            copy per batch item and tensor when the heads of a row, or the
+ *            rows of a head, are contiguous.
+ *  causal  : 0 or 1 as for sage_attention.
+ *  head_groups : 1 .. H.
+ *  buf     : full-size buffers as for sage_prep_qkv (each range uses its own
+ *            heads' slices).  Lengths are taken as all valid.
+ * The work is ordered after prior work on `stream` and later work on
+ * `stream` waits for all of it; the call does not synchronize.  The internal
+ * streams and events are created on the first call on a device and kept.
+ * The output equals sage_prep_qkv + sage_attn_fwd[_causal] on the same
+ * inputs bit for bit.  SAGE_ERR_ARG for a NULL host pointer, mismatched
+ * strides or head_groups out of range. */
+int sage_attention_host_overlapped(const sage_tensor* q_host, const sage_tensor* k_host,
+                                   const sage_tensor* v_host, const sage_tensor* o_host,
+                                   const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
+                                   const sage_tensor* o, int B, int H, int Nq, int Nkv, int D,
+                                   float sm_scale, int causal, int head_groups,
+                                   const sage_prep_buffers* buf, void* stream);
+
 /* Synchronizes the device, returns the first error a kernel recorded since
  * the last call (SAGE_OK if none) and clears it. */
 int sage_get_device_status(void);

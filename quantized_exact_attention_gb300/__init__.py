@@ -31,6 +31,7 @@ HEAD_DIMS = (64, 128)       # head dimensions the kernels are built for
 # Names the header declares (checked by the CPU tests against the .so exports).
 EXPORTED = ("sage_buffer_sizes", "sage_prep_qkv", "sage_attn_fwd", "sage_attn_fwd_causal", "sage_attention",
             "sage_attn_checkpoints", "sage_prep_qkv_bkv", "sage_attn_fwd_bkv", "sage_set_cta_pairing",
+            "sage_attention_host_overlapped",
             "sage_qk_int32",
             "sage_attention_host", "sage_get_device_status", "sage_status_string",
             "sage_last_launch_count", "sage_debug_inject_fault", "sage_prep_qkv_noalloc",
@@ -105,6 +106,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sage_last_launch_count.argtypes = []
     lib.sage_debug_inject_fault.argtypes = [i]
     lib.sage_set_cta_pairing.argtypes = [i]
+    lib.sage_attention_host_overlapped.argtypes = [P(sage_tensor)] * 8 + [i, i, i, i, i, f, i, i,
+                                                                          P(sage_prep_buffers), vp]
     lib.sage_prep_qkv_noalloc.argtypes = lib.sage_prep_qkv.argtypes
     lib.sage_prep_noalloc_capacity.argtypes = []
     for name in EXPORTED:
@@ -306,6 +309,22 @@ def sage_attention_host(host_phys, dev_phys, views_of, bufs: PrepBuffers, o_dev,
                                             ctypes.byref(pb), ctypes.byref(os_), ctypes.byref(out),
                                             B, H, Nq, Nkv, D, float(sm_scale), _stream_ptr(stream))
     _check(rc, "sage_attention_host")
+
+
+def sage_attention_host_overlapped(q_host, k_host, v_host, o_host, q, k, v, o, bufs: PrepBuffers,
+                                   sm_scale: float = 0.0, causal: bool = False, head_groups: int = 4,
+                                   stream=None):
+    """End-to-end call with copies overlapped with compute: host views
+    q_host.. (pinned, same strides as the device views q..), per head range
+    copy in, prep, attention, copy out."""
+    B, H, Nq, D = q.shape
+    Nkv = k.shape[2]
+    descs = [tensor_desc(t) for t in (q_host, k_host, v_host, o_host, q, k, v, o)]
+    pb = bufs.c_struct()
+    rc = load_library().sage_attention_host_overlapped(*[ctypes.byref(d) for d in descs], B, H, Nq, Nkv, D,
+                                                       float(sm_scale), 1 if causal else 0, int(head_groups),
+                                                       ctypes.byref(pb), _stream_ptr(stream))
+    _check(rc, "sage_attention_host_overlapped")
 
 
 def sage_get_device_status() -> int:

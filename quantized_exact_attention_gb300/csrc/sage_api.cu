@@ -151,7 +151,7 @@ int sage_buffer_sizes(int B, int H, int Nq, int Nkv, int D, sage_sizes* out) {
 
 static int prep_common(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v, int B, int H, int Nq,
                        int Nkv, int D, const int32_t* q_len, const int32_t* kv_len, float sv,
-                       const sage_prep_buffers* out, void* stream) {
+                       const sage_prep_buffers* out, void* stream, int h_begin = 0, int h_count = -1) {
     int rc = check_shape(B, H, Nq, Nkv, D);
     if (rc != SAGE_OK) return rc;
     if ((rc = check_tensor(q)) != SAGE_OK || (rc = check_tensor(k)) != SAGE_OK || (rc = check_tensor(v)) != SAGE_OK)
@@ -167,7 +167,8 @@ static int prep_common(const sage_tensor* q, const sage_tensor* k, const sage_te
     p.qsb = q->stride_b; p.qsh = q->stride_h; p.qsn = q->stride_n;
     p.ksb = k->stride_b; p.ksh = k->stride_h; p.ksn = k->stride_n;
     p.vsb = v->stride_b; p.vsh = v->stride_h; p.vsn = v->stride_n;
-    p.B = B; p.H = H; p.Nq = Nq; p.Nkv = Nkv; p.D = D; p.sv = sv;
+    p.B = B; p.H = H; p.h_begin = h_begin; p.h_count = h_count < 0 ? H : h_count;
+    p.Nq = Nq; p.Nkv = Nkv; p.D = D; p.sv = sv;
     p.nkv_pad = (int)sz.nkv_pad;
     p.nq_blocks = (int)ceil_div(Nq, kBQS);
     p.nk_blocks = (int)ceil_div(Nkv, kBKS);
@@ -207,7 +208,7 @@ int sage_prep_qkv_bkv(const sage_tensor* q, const sage_tensor* k, const sage_ten
 static int attn_common(const sage_prep_buffers* in, const sage_tensor* o, int32_t* s_out, int B, int H, int Nq,
                        int Nkv, int D, const int32_t* q_len, const int32_t* kv_len, float sm_scale,
                        void* stream, bool capture, bool causal, const CkptParams* ck = nullptr,
-                       bool bkv64 = false) {
+                       bool bkv64 = false, int h_begin = 0, int h_count = -1) {
     int rc = check_shape(B, H, Nq, Nkv, D);
     if (rc != SAGE_OK) return rc;
     sage_sizes sz;
@@ -245,7 +246,8 @@ static int attn_common(const sage_prep_buffers* in, const sage_tensor* o, int32_
         p.osb = o->stride_b; p.osh = o->stride_h; p.osn = o->stride_n;
     }
     p.s_out = s_out;
-    p.B = B; p.H = H; p.Nq = Nq; p.Nkv = Nkv; p.D = D;
+    p.B = B; p.H = H; p.h_begin = h_begin; p.h_count = h_count < 0 ? H : h_count;
+    p.Nq = Nq; p.Nkv = Nkv; p.D = D;
     p.nq_blocks = (int)ceil_div(Nq, kBQS);
     p.nk_blocks = (int)ceil_div(Nkv, kBKS);
     const double scale = sm_scale > 0.f ? (double)sm_scale : 1.0 / std::sqrt((double)D);
@@ -338,7 +340,7 @@ int sage_attention(const sage_tensor* q, const sage_tensor* k, const sage_tensor
     pp.v = static_cast<const uint16_t*>(v->ptr);
     pp.ksb = k->stride_b; pp.ksh = k->stride_h; pp.ksn = k->stride_n;
     pp.vsb = v->stride_b; pp.vsh = v->stride_h; pp.vsn = v->stride_n;
-    pp.B = B; pp.H = H; pp.Nq = Nq; pp.Nkv = Nkv; pp.D = D; pp.sv = kSV;
+    pp.B = B; pp.H = H; pp.h_begin = 0; pp.h_count = H; pp.Nq = Nq; pp.Nkv = Nkv; pp.D = D; pp.sv = kSV;
     pp.nkv_pad = (int)sz.nkv_pad;
     pp.nq_blocks = (int)ceil_div(Nq, kBQS);
     pp.nk_blocks = (int)ceil_div(Nkv, kBKS);
@@ -370,7 +372,7 @@ int sage_attention(const sage_tensor* q, const sage_tensor* k, const sage_tensor
     p.q_len = q_len; p.kv_len = kv_len;
     p.o = static_cast<uint16_t*>(const_cast<void*>(o->ptr));
     p.osb = o->stride_b; p.osh = o->stride_h; p.osn = o->stride_n;
-    p.B = B; p.H = H; p.Nq = Nq; p.Nkv = Nkv; p.D = D;
+    p.B = B; p.H = H; p.h_begin = 0; p.h_count = H; p.Nq = Nq; p.Nkv = Nkv; p.D = D;
     p.nq_blocks = pp.nq_blocks;
     p.nk_blocks = pp.nk_blocks;
     const double scale = sm_scale > 0.f ? (double)sm_scale : 1.0 / std::sqrt((double)D);
@@ -412,6 +414,107 @@ int sage_attention_host(const sage_copy* inputs, int n_inputs, const sage_tensor
                         s) != cudaSuccess)
         return SAGE_ERR_LAUNCH;
     return SAGE_OK;
+}
+
+// Copy heads [h0, h0 + nh) of a [B, H, N, D] BF16 tensor (element strides of
+// t; the same physical layout on both sides) with 2-D copies.
+static int copy_heads(void* dst, const void* src, const sage_tensor* t, int B, int N, int D, int h0, int nh,
+                      cudaMemcpyKind kind, cudaStream_t s) {
+    const int64_t sb = t->stride_b, sh = t->stride_h, sn = t->stride_n;
+    for (int b = 0; b < B; ++b) {
+        const int64_t off = (b * sb + (int64_t)h0 * sh) * 2;
+        char* d = static_cast<char*>(dst) + off;
+        const char* c = static_cast<const char*>(src) + off;
+        cudaError_t e;
+        if (sh == D && sn >= (int64_t)nh * D)          // a row holds the head range contiguously
+            e = cudaMemcpy2DAsync(d, sn * 2, c, sn * 2, (size_t)nh * D * 2, (size_t)N, kind, s);
+        else if (sn == D && sh >= (int64_t)N * D)      // each head is one contiguous block
+            e = cudaMemcpy2DAsync(d, sh * 2, c, sh * 2, (size_t)N * D * 2, (size_t)nh, kind, s);
+        else {
+            e = cudaSuccess;
+            for (int h = 0; h < nh && e == cudaSuccess; ++h)
+                e = cudaMemcpy2DAsync(d + h * sh * 2, sn * 2, c + h * sh * 2, sn * 2, (size_t)D * 2, (size_t)N, kind,
+                                      s);
+        }
+        if (e != cudaSuccess) return SAGE_ERR_LAUNCH;
+    }
+    return SAGE_OK;
+}
+
+// Streams and events of the overlapped host entry, created once per device.
+struct OverlapStreams {
+    cudaStream_t s[3] = {};
+    cudaEvent_t start = nullptr, done[3] = {};
+    bool ready = false;
+};
+static OverlapStreams g_overlap[64];
+
+static OverlapStreams* overlap_streams() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    OverlapStreams& o = g_overlap[dev];
+    if (!o.ready) {
+        for (int i = 0; i < 3; ++i)
+            if (cudaStreamCreateWithFlags(&o.s[i], cudaStreamNonBlocking) != cudaSuccess ||
+                cudaEventCreateWithFlags(&o.done[i], cudaEventDisableTiming) != cudaSuccess)
+                return nullptr;
+        if (cudaEventCreateWithFlags(&o.start, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+        o.ready = true;
+    }
+    return &o;
+}
+
+int sage_attention_host_overlapped(const sage_tensor* q_host, const sage_tensor* k_host, const sage_tensor* v_host,
+                                   const sage_tensor* o_host, const sage_tensor* q, const sage_tensor* k,
+                                   const sage_tensor* v, const sage_tensor* o, int B, int H, int Nq, int Nkv, int D,
+                                   float sm_scale, int causal, int head_groups, const sage_prep_buffers* buf,
+                                   void* stream) {
+    int rc = check_shape(B, H, Nq, Nkv, D);
+    if (rc != SAGE_OK) return rc;
+    if (head_groups < 1 || head_groups > H) return SAGE_ERR_ARG;
+    const sage_tensor* hs[4] = {q_host, k_host, v_host, o_host};
+    const sage_tensor* ds[4] = {q, k, v, o};
+    for (int i = 0; i < 4; ++i) {
+        if (hs[i] == nullptr || hs[i]->ptr == nullptr) return SAGE_ERR_ARG;
+        if ((rc = check_tensor(ds[i])) != SAGE_OK) return rc;
+        if (hs[i]->stride_b != ds[i]->stride_b || hs[i]->stride_h != ds[i]->stride_h ||
+            hs[i]->stride_n != ds[i]->stride_n)
+            return SAGE_ERR_ARG;
+    }
+    OverlapStreams* os = overlap_streams();
+    if (os == nullptr) return SAGE_ERR_LAUNCH;
+    cudaStream_t user = static_cast<cudaStream_t>(stream);
+    if (cudaEventRecord(os->start, user) != cudaSuccess) return SAGE_ERR_LAUNCH;
+    for (int i = 0; i < 3; ++i)
+        if (cudaStreamWaitEvent(os->s[i], os->start, 0) != cudaSuccess) return SAGE_ERR_LAUNCH;
+    int launches = 0;
+    for (int g = 0; g < head_groups && rc == SAGE_OK; ++g) {
+        const int h0 = (int)((int64_t)H * g / head_groups), h1 = (int)((int64_t)H * (g + 1) / head_groups);
+        cudaStream_t s = os->s[g % 3];
+        if ((rc = copy_heads(const_cast<void*>(q->ptr), q_host->ptr, q, B, Nq, D, h0, h1 - h0,
+                             cudaMemcpyHostToDevice, s)) != SAGE_OK ||
+            (rc = copy_heads(const_cast<void*>(k->ptr), k_host->ptr, k, B, Nkv, D, h0, h1 - h0,
+                             cudaMemcpyHostToDevice, s)) != SAGE_OK ||
+            (rc = copy_heads(const_cast<void*>(v->ptr), v_host->ptr, v, B, Nkv, D, h0, h1 - h0,
+                             cudaMemcpyHostToDevice, s)) != SAGE_OK)
+            break;
+        rc = prep_common(q, k, v, B, H, Nq, Nkv, D, nullptr, nullptr, kSV, buf, s, h0, h1 - h0);
+        if (rc != SAGE_OK) break;
+        launches += g_last_launches;
+        rc = attn_common(buf, o, nullptr, B, H, Nq, Nkv, D, nullptr, nullptr, sm_scale, s, false, causal != 0,
+                         nullptr, false, h0, h1 - h0);
+        if (rc != SAGE_OK) break;
+        launches += g_last_launches;
+        rc = copy_heads(const_cast<void*>(o_host->ptr), o->ptr, o, B, Nq, D, h0, h1 - h0, cudaMemcpyDeviceToHost, s);
+    }
+    // the caller's stream resumes after every group, also on an error
+    for (int i = 0; i < 3; ++i) {
+        if (cudaEventRecord(os->done[i], os->s[i]) != cudaSuccess) return SAGE_ERR_LAUNCH;
+        if (cudaStreamWaitEvent(user, os->done[i], 0) != cudaSuccess) return SAGE_ERR_LAUNCH;
+    }
+    if (rc == SAGE_OK) g_last_launches = launches;
+    return rc;
 }
 
 int sage_get_device_status(void) {

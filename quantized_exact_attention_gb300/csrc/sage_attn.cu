@@ -187,7 +187,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // causal: the longest query tiles start first
         qtile = kCkpt ? p.ck.qtile : (kCausal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x);
     }
-    const int h = kCkpt ? p.ck.h : (int)blockIdx.y, b = kCkpt ? p.ck.b : (int)blockIdx.z;
+    const int h = kCkpt ? p.ck.h : p.h_begin + (int)blockIdx.y, b = kCkpt ? p.ck.b : (int)blockIdx.z;
     const int bh = b * p.H + h;
     const int q0 = qtile * 128;
     const int lq = clamp_len(p.q_len, b, p.Nq);
@@ -786,7 +786,7 @@ cudaError_t launch_one(const AttnParams& p, const CUtensorMap& tq, const CUtenso
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    const dim3 grid = kCkpt ? dim3(1, 1, 1) : dim3((unsigned)((p.Nq + 127) / 128), (unsigned)p.H, (unsigned)p.B);
+    const dim3 grid = kCkpt ? dim3(1, 1, 1) : dim3((unsigned)((p.Nq + 127) / 128), (unsigned)p.h_count, (unsigned)p.B);
     sage_attn_kernel<D, kCapture, kCausal, kFusedQ, kCkpt, kB64><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
@@ -808,7 +808,7 @@ cudaError_t launch_pair(const AttnParams& p, const CUtensorMap& tq, const CUtens
     }
     const unsigned pairs = (unsigned)((p.Nq + 255) / 256);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * pairs, (unsigned)p.H, (unsigned)p.B);
+    cfg.gridDim = dim3(2 * pairs, (unsigned)p.h_count, (unsigned)p.B);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = s;

@@ -26,6 +26,7 @@ struct PrepParams {
     const uint16_t* v;
     int64_t qsb, qsh, qsn, ksb, ksh, ksn, vsb, vsh, vsn;   // element strides
     int B, H, Nq, Nkv, D, nkv_pad;         // D: head dimension, 64 or 128
+    int h_begin, h_count;                  // heads [h_begin, h_begin + h_count) are processed
     int nq_blocks, nk_blocks, n_chunks;    // ceil(Nq/128), ceil(Nkv/64), ceil(Nkv/64)
     const int32_t* q_len;                  // device [B] or null
     const int32_t* kv_len;
@@ -66,6 +67,7 @@ struct AttnParams {
     int64_t osb, osh, osn;
     int32_t* s_out;                        // QK checkpoint output (capture kernel only)
     int B, H, Nq, Nkv, D;                  // D: head dimension, 64 or 128
+    int h_begin, h_count;                  // heads [h_begin, h_begin + h_count) are processed
     int nq_blocks, nk_blocks;
     float c;                               // fp32(sm_scale * log2(e))
     int* status;                           // device status words

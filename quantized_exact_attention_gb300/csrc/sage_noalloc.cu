@@ -92,7 +92,7 @@ extern "C" int sage_prep_qkv_noalloc(const sage_tensor* q, const sage_tensor* k,
     p.qsb = q->stride_b; p.qsh = q->stride_h; p.qsn = q->stride_n;
     p.ksb = k->stride_b; p.ksh = k->stride_h; p.ksn = k->stride_n;
     p.vsb = v->stride_b; p.vsh = v->stride_h; p.vsn = v->stride_n;
-    p.B = B; p.H = H; p.Nq = Nq; p.Nkv = Nkv; p.D = D; p.sv = kSV;
+    p.B = B; p.H = H; p.h_begin = 0; p.h_count = H; p.Nq = Nq; p.Nkv = Nkv; p.D = D; p.sv = kSV;
     p.nkv_pad = (int)sz.nkv_pad;
     p.nq_blocks = (int)ceil_div(Nq, kBQS);
     p.nk_blocks = (int)ceil_div(Nkv, kBKS);

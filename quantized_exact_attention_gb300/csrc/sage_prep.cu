@@ -170,7 +170,7 @@ template <int D>
 __global__ void __launch_bounds__(256, 3) prep_stats_q_kernel(const PrepParams p) {
     using Sh = PrepShape<D>;
     __shared__ float red[8];
-    const int b = blockIdx.z, h = blockIdx.y;
+    const int b = blockIdx.z, h = p.h_begin + (int)blockIdx.y;
     const int n_stat_blocks = (p.n_chunks + Sh::kStatChunks - 1) / Sh::kStatChunks;
     if ((int)blockIdx.x < n_stat_blocks) {
         const int c = blockIdx.x * Sh::kStatChunks + (threadIdx.x / Sh::kGroups);
@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(256, 3) prep_stats_q_kernel(const PrepParams p
 // ---------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(128) prep_finalize_kernel(const PrepParams p) {
-    const int b = blockIdx.y, h = blockIdx.x, d = threadIdx.x;
+    const int b = blockIdx.y, h = p.h_begin + (int)blockIdx.x, d = threadIdx.x;
     const int lk = clamp_len(p.kv_len, b, p.Nkv);
     const int nc = (lk + kMeanChunk - 1) / kMeanChunk;
     const int64_t base = ((int64_t)b * p.H + h) * p.n_chunks * D + d;
@@ -331,7 +331,7 @@ template <int D>
 __global__ void __launch_bounds__(256, 4) prep_kv_kernel(const PrepParams p) {
     __shared__ float red[8];
     __shared__ __align__(16) uint32_t vtile[D * PrepShape<D>::kVStride];   // [d][words of 4 tokens + 4 pad]
-    const int b = blockIdx.z, h = blockIdx.y;
+    const int b = blockIdx.z, h = p.h_begin + (int)blockIdx.y;
     if ((int)blockIdx.x < p.nk_blocks) quant_k_block<D>(p, b, h, blockIdx.x, red);
     else quant_v_tile<D>(p, b, h, blockIdx.x - p.nk_blocks, vtile);
 }
@@ -344,18 +344,18 @@ cudaError_t launch_prep_d(const PrepParams& p, bool with_q, cudaStream_t s, int*
         // Q blocks follow the statistics blocks in the grid; without Q they are
         // simply not launched
         const int n_stat_blocks = (p.n_chunks + Sh::kStatChunks - 1) / Sh::kStatChunks;
-        dim3 grid((unsigned)(n_stat_blocks + (with_q ? p.nq_blocks : 0)), (unsigned)p.H, (unsigned)p.B);
+        dim3 grid((unsigned)(n_stat_blocks + (with_q ? p.nq_blocks : 0)), (unsigned)p.h_count, (unsigned)p.B);
         prep_stats_q_kernel<D><<<grid, 256, 0, s>>>(p);
         ++*launches;
     }
     {
-        dim3 grid((unsigned)p.H, (unsigned)p.B);
+        dim3 grid((unsigned)p.h_count, (unsigned)p.B);
         prep_finalize_kernel<D><<<grid, D, 0, s>>>(p);
         ++*launches;
     }
     {
         const int n_vtiles = (p.nkv_pad + Sh::kVTokens - 1) / Sh::kVTokens;
-        dim3 grid((unsigned)(p.nk_blocks + n_vtiles), (unsigned)p.H, (unsigned)p.B);
+        dim3 grid((unsigned)(p.nk_blocks + n_vtiles), (unsigned)p.h_count, (unsigned)p.B);
         prep_kv_kernel<D><<<grid, 256, 0, s>>>(p);
         ++*launches;
     }
