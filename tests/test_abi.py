@@ -130,6 +130,23 @@ def test_fused_entry_and_causal_reject_bad_arguments_before_touching_the_gpu(lib
                                     None, 0.0, None) == S.SAGE_ERR_UNSUPPORTED
 
 
+def test_overlapped_host_entry_rejects_bad_arguments_before_touching_the_gpu(lib):
+    t = _fake_tensor()
+    b = _fake_bufs()
+
+    def call(hq=t, dq=t, groups=4, shape=(1, 8, 256, 256, 128)):
+        tens = [hq, t, t, t, dq, t, t, t]
+        return lib.sage_attention_host_overlapped(*[ctypes.byref(x) for x in tens], *shape, 0.0, 0, groups,
+                                                  ctypes.byref(b), None)
+
+    assert call(groups=0) == S.SAGE_ERR_ARG
+    assert call(groups=9) == S.SAGE_ERR_ARG                     # more ranges than heads
+    assert call(hq=_fake_tensor(ptr=0)) == S.SAGE_ERR_ARG
+    assert call(hq=_fake_tensor(sn=128 * 8)) == S.SAGE_ERR_ARG  # host strides differ from the device view's
+    assert call(dq=_fake_tensor(ptr=0x10004)) == S.SAGE_ERR_UNSUPPORTED
+    assert call(shape=(1, 8, 256, 256, 96)) == S.SAGE_ERR_UNSUPPORTED
+
+
 def test_status_strings(lib):
     for code in (0, -1, -2, -3, -4, -5):
         assert S.status_string(code) not in ("", "unknown status")
