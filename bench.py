@@ -10,6 +10,8 @@ larger than the 129 MB L2, so no L2 flush is needed between steps.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
   python bench.py --forms     # one JSON line per form of the path (not the
                               # contract line): causal, fused entry, BKV = 64, D = 64
+  python bench.py --latency   # p50 latency on the single-tile workload (Q128 x KV192 x
+                              # D128, the pages' prototype shape); not the contract line
 
 --impl reference times the CPU oracle (the only other implementation of the
 contract; no other implementation exists to install) on a bounded sample of
@@ -50,6 +52,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--forms", action="store_true",
                     help="time every form of the path on the bench workload shape instead")
+    ap.add_argument("--latency", action="store_true",
+                    help="p50 latency of prep + attention on the single-tile workload instead")
     return ap.parse_args()
 
 
@@ -450,9 +454,53 @@ def run_forms(args):
         torch.cuda.empty_cache()
 
 
+def run_latency(args):
+    """p50 over many calls of each entry on the single-tile workload; each call
+    is timed alone (events around it, a synchronize after)."""
+    import torch
+
+    import quantized_exact_attention_gb300 as S
+    from quantized_exact_attention_gb300 import build as B
+    from quantized_exact_attention_gb300 import workloads as W
+
+    B.build()
+    S.load_library()
+    w = W.make_config(1)
+    phys = w.to("cuda")
+    q, k, v = w.views(phys)
+    bufs = S.alloc_prep_buffers(w.B, w.H, w.Nq, w.Nkv, "cuda")
+    o = torch.empty((w.B, w.Nq, w.H, w.D), dtype=torch.bfloat16, device="cuda").permute(0, 2, 1, 3)
+    S.sage_prep_qkv(q, k, v, bufs)
+    calls = {"attention (sage_attn_fwd)": lambda: S.sage_attn_fwd(bufs, o),
+             "prep + attention (sage_prep_qkv, sage_attn_fwd)": lambda: (S.sage_prep_qkv(q, k, v, bufs),
+                                                                        S.sage_attn_fwd(bufs, o)),
+             "one call (sage_attention)": lambda: S.sage_attention(q, k, v, o, bufs)}
+    n = max(20, args.steps)
+    for name, fn in calls.items():
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(n):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        print(json.dumps({"workload": w.name, "entry": name, "p50_ms": statistics.median(ts),
+                          "min_ms": min(ts), "calls": n}), flush=True)
+    if S.sage_get_device_status() != S.SAGE_OK:
+        raise RuntimeError("device status reports an error")
+
+
 def main():
     args = parse_args()
     world, rank, local = dist_env()
+    if args.latency:
+        if rank == 0:
+            run_latency(args)
+        return
     if args.forms:
         if rank == 0:
             run_forms(args)
