@@ -6,8 +6,8 @@
 //   1. prep_stats_q   per 64-token chunk: ordered FP32 K column sums and V
 //                     column |max| (16 chunks per block); and, independent
 //                     of those, the INT8 quantization of every 128-row Q block
-//   2. prep_finalize  per (b,h): chunk sums in order -> K mean; V amax ->
-//                     v_scale and its inverse
+//   2. prep_finalize  per (b,h) and 16 channels: chunk sums in order -> K
+//                     mean; V amax -> v_scale and its inverse
 //   3. prep_kv        K blocks (64 rows of K - mean) and V tiles (64 tokens,
 //                     written transposed: token index fastest)
 // Loaded BF16 data stays packed in registers (8 values per 16-byte word) and
@@ -181,41 +181,50 @@ __global__ void __launch_bounds__(256, 3) prep_stats_q_kernel(const PrepParams p
 }
 
 // ---------------------------------------------------------------------------
-// 2. Per-(b,h) finalisation, one thread per channel.  The chunk partials are
-// fetched 32 at a time (independent loads in flight) and then added strictly
-// in ascending chunk order.
+// 2. Per-(b,h) finalisation.  A block owns 16 channels of one head: its 256
+// threads stage the chunk partials of those channels in shared memory (256
+// chunks per pass, every load in flight at once), then one thread per
+// channel adds them strictly in ascending chunk order.
 // ---------------------------------------------------------------------------
+constexpr int kFinChannels = 16;
+constexpr int kFinChunks = 256;            // chunks staged per pass
+
 template <int D>
-__global__ void __launch_bounds__(128) prep_finalize_kernel(const PrepParams p) {
-    const int b = blockIdx.y, h = p.h_begin + (int)blockIdx.x, d = threadIdx.x;
+__global__ void __launch_bounds__(256) prep_finalize_kernel(const PrepParams p) {
+    __shared__ __align__(16) float st_sum[kFinChunks * kFinChannels];
+    __shared__ __align__(16) float st_max[kFinChunks * kFinChannels];
+    const int b = blockIdx.z, h = p.h_begin + (int)blockIdx.y, d0 = blockIdx.x * kFinChannels;
     const int lk = clamp_len(p.kv_len, b, p.Nkv);
     const int nc = (lk + kMeanChunk - 1) / kMeanChunk;
-    const int64_t base = ((int64_t)b * p.H + h) * p.n_chunks * D + d;
-    const float* ps = p.psum + base;
-    const float* pa = p.pamax + base;
+    const int64_t base = ((int64_t)b * p.H + h) * p.n_chunks * D + d0;
+    const int quad = threadIdx.x & 3, lane_c = threadIdx.x >> 2;       // 4 float4 per chunk row, 64 chunk lanes
     float total = 0.f, amax = 0.f;
-    int c = 0;
-    for (; c + 32 <= nc; c += 32) {
-        float sv[32], av[32];
+    for (int c0 = 0; c0 < nc; c0 += kFinChunks) {
+        const int n = min(kFinChunks, nc - c0);
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-            sv[u] = ps[(int64_t)(c + u) * D];
-            av[u] = pa[(int64_t)(c + u) * D];
+        for (int i = 0; i < kFinChunks / 64; ++i) {
+            const int c = lane_c + 64 * i;
+            if (c < n) {
+                const int64_t g = base + (int64_t)(c0 + c) * D + quad * 4;
+                reinterpret_cast<float4*>(st_sum)[c * 4 + quad] = __ldcg(reinterpret_cast<const float4*>(p.psum + g));
+                reinterpret_cast<float4*>(st_max)[c * 4 + quad] = __ldcg(reinterpret_cast<const float4*>(p.pamax + g));
+            }
         }
-#pragma unroll
-        for (int u = 0; u < 32; ++u) {
-            total = __fadd_rn(total, sv[u]);
-            amax = fmaxf(amax, av[u]);
+        __syncthreads();
+        if (threadIdx.x < kFinChannels) {
+            for (int c = 0; c < n; ++c) {
+                total = __fadd_rn(total, st_sum[c * kFinChannels + threadIdx.x]);
+                amax = fmaxf(amax, st_max[c * kFinChannels + threadIdx.x]);
+            }
         }
+        __syncthreads();
     }
-    for (; c < nc; ++c) {
-        total = __fadd_rn(total, ps[(int64_t)c * D]);
-        amax = fmaxf(amax, pa[(int64_t)c * D]);
+    if (threadIdx.x < kFinChannels) {
+        const int64_t o = ((int64_t)b * p.H + h) * D + d0 + threadIdx.x;
+        p.k_mean[o] = lk > 0 ? __fdiv_rn(total, (float)lk) : 0.f;
+        p.v_scale[o] = amax > 0.f ? __fdiv_rn(amax, p.sv) : 0.f;
+        p.v_inv[o] = amax > 0.f ? __fdiv_rn(p.sv, amax) : 0.f;
     }
-    const int64_t o = ((int64_t)b * p.H + h) * D + d;
-    p.k_mean[o] = lk > 0 ? __fdiv_rn(total, (float)lk) : 0.f;
-    p.v_scale[o] = amax > 0.f ? __fdiv_rn(amax, p.sv) : 0.f;
-    p.v_inv[o] = amax > 0.f ? __fdiv_rn(p.sv, amax) : 0.f;
 }
 
 // ---------------------------------------------------------------------------
@@ -349,8 +358,8 @@ cudaError_t launch_prep_d(const PrepParams& p, bool with_q, cudaStream_t s, int*
         ++*launches;
     }
     {
-        dim3 grid((unsigned)p.h_count, (unsigned)p.B);
-        prep_finalize_kernel<D><<<grid, D, 0, s>>>(p);
+        dim3 grid((unsigned)(D / kFinChannels), (unsigned)p.h_count, (unsigned)p.B);
+        prep_finalize_kernel<D><<<grid, 256, 0, s>>>(p);
         ++*launches;
     }
     {
