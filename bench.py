@@ -57,19 +57,27 @@ def parse_args():
     return ap.parse_args()
 
 
+def sources_sha256(paths):
+    """SHA-256 over the given repository files, concatenated in order."""
+    import hashlib
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def kernel_traffic():
     """DRAM bytes per launch of the attention kernel from the committed ncu
-    capture (profiles/sage_attn_kernel_counters.json), or None when the
-    kernel source has changed since the counters were taken."""
-    import hashlib
+    capture (profiles/sage_attn_kernel_counters.json), or None when any source
+    the kernel is compiled from has changed since the counters were taken."""
     try:
         with open(os.path.join(ROOT, "profiles", "sage_attn_kernel_counters.json")) as f:
             rec = json.load(f)
-        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()
-    except (OSError, KeyError, ValueError):
+        sha = sources_sha256(rec["sources"])
+    except (OSError, KeyError, ValueError, TypeError):
         return None
-    if sha != rec.get("source_sha256"):
+    if sha != rec.get("sources_sha256"):
         return None
     return int(rec["dram_bytes_read"]) + int(rec["dram_bytes_write"])
 

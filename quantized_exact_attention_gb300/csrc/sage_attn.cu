@@ -228,6 +228,12 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     auto wwait = [&](uint32_t bb, uint32_t par, const volatile int* af) -> bool {
         return __all_sync(0xffffffffu, bwait(bb, par, af));
     };
+    // Waits off the critical chain (the correction's alpha wait, the producer's
+    // ring-slot waits) sleep between checks; the others spin.
+    auto swait = [&](uint32_t bb, uint32_t par, const volatile int* af) -> bool {
+        if constexpr (kPair) return mbar_wait_cluster(bb, par, af);
+        else return mbar_wait_sleep(bb, par, af);
+    };
     auto commit = [&](uint32_t bb) {
         if constexpr (kPair) mma_commit2(bb);
         else mma_commit(bb);
@@ -511,7 +517,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             bool ok = true;
             for (int t = 0; t < T; ++t) {
                 const int sb = t & 1;
-                if (!wwait(bar(B_AFULL + sb), (t >> 1) & 1, abort_flag)) {
+                if (!__all_sync(0xffffffffu, swait(bar(B_AFULL + sb), (t >> 1) & 1, abort_flag))) {
                     if (lane == 0) fail(R_CORRECT, t);
                     ok = false;
                     break;
@@ -616,7 +622,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
             auto load_k = [&](int t) -> bool {
                 const int st = t % kNK;
-                if (t >= kNK && !bwait(bar(B_KEMPTY + st), ((t / kNK) - 1) & 1, abort_flag)) return false;
+                if (t >= kNK && !swait(bar(B_KEMPTY + st), ((t / kNK) - 1) & 1, abort_flag)) return false;
                 const uint32_t dst = sbase + OFF_K + st * kTileKBytes;
                 if (rank == 0) mbar_arrive_expect_tx(bar(B_KFULL + st), (kPair ? 2 : 1) * kTileKBytes);
 #pragma unroll
@@ -632,7 +638,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             };
             auto load_v = [&](int t) -> bool {
                 const int st = t % kNV;
-                if (t >= kNV && !bwait(bar(B_VEMPTY + st), ((t / kNV) - 1) & 1, abort_flag)) return false;
+                if (t >= kNV && !swait(bar(B_VEMPTY + st), ((t / kNV) - 1) & 1, abort_flag)) return false;
                 const uint32_t dst = sbase + OFF_V + st * kTileVBytes;
                 if (rank == 0) mbar_arrive_expect_tx(bar(B_VFULL + st), (kPair ? 2 : 1) * kTileVBytes);
                 if (p.fault_mode != 1) {

@@ -63,6 +63,31 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
     }
 }
 
+// The same bounded wait with a suspend-time hint: between checks the thread
+// may sleep until the phase completes (or 200 ns pass), so its polling does
+// not take issue slots from the warps it shares a scheduler with.  Waking
+// costs latency, so this form is for waits off the critical chain.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(bar), "r"(parity), "n"(200) : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait_sleep(bar, parity)) return true;
+        if ((i & 15u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > kWaitLimitNs) return false;
+        }
+    }
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
