@@ -30,7 +30,10 @@
 // P of a tile overwriting the first 32 columns of its S buffer (4 values per
 // 32-bit column), and one PV buffer [384,512) of FP16 tile sums (one per
 // column).  Three S/P buffers let QK run two tiles ahead of PV, so the
-// softmax of tile t+1 never waits for the PV MMA of tile t-1.
+// softmax of tile t+1 never waits for the PV MMA of tile t-1.  The BKV = 64
+// form instead has two S/P buffers [0,256) and two PV buffers [256,512), one
+// per 64-key epoch, so the PV of an epoch waits only for the drain of the
+// same epoch one tile earlier.
 //
 // Every mbarrier wait is bounded (sage_ptx.cuh); a wait that runs out records
 // SAGE_ERR_TIMEOUT in the device status words, raises a CTA-wide abort flag,
@@ -64,7 +67,7 @@ enum Bar : uint32_t {
     B_SFULL = B_VEMPTY + kNV,   // [3] S/P buffers
     B_SFREE = B_SFULL + kNS,
     B_PFULL = B_SFREE + kNS,
-    B_PVFULL = B_PFULL + kNS,   // single PV buffer
+    B_PVFULL = B_PFULL + kNS,   // PV buffer 0 (the only one except with BKV = 64)
     B_PVFREE = B_PVFULL + 1,
     B_AFULL = B_PVFREE + 1,
     B_AFREE = B_AFULL + 2,
@@ -104,7 +107,7 @@ struct Smem {
 };
 
 constexpr uint32_t TM_S = 0;        // S buffer b (0..2) at column 128*b
-constexpr uint32_t TM_PV = 384;     // PV buffer (D FP16 tile sums, one per column)
+constexpr uint32_t TM_PV = 384;     // PV buffer (D FP16 tile sums, one per column); BKV = 64: 256 + 128*epoch
 // P of tile t is written over the first 32 columns of S buffer t%2 once both
 // halves of every row have read their S values; the next QK into that buffer
 // is issued after the PV MMA that reads P, and tcgen05.mma executes in issue
@@ -238,6 +241,17 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if constexpr (kPair) mma_commit2(bb);
         else mma_commit(bb);
     };
+    // BKV = 64 (not paired): two PV buffers, one per epoch, so that the PV of
+    // epoch e waits only for the drain of epoch e of the previous tile; the
+    // S/P buffers are then two.
+    constexpr bool kDB = kB64 && !kPair;
+    static_assert(!(kB64 && kFusedQ), "the BKV = 64 form has no fused Q prologue (its scratch holds PV barriers)");
+    constexpr int kNSb = kDB ? 2 : kNS;
+    auto tm_pv = [&](int j) -> uint32_t { return kDB ? 256u + 128u * (uint32_t)j : TM_PV; };
+    // PV buffer j's barriers; buffer 1's (BKV = 64 only) live in the scratch of
+    // the fused-Q prologue, which that form never runs
+    auto pv_full = [&](int j) -> uint32_t { return (kDB && j) ? sbase + OFF_RED : bar(B_PVFULL); };
+    auto pv_free = [&](int j) -> uint32_t { return (kDB && j) ? sbase + OFF_RED + 8u : bar(B_PVFREE); };
     auto fail = [&](int role, int tile) {
         record_failure(p, abort_flag, role, tile);
         if constexpr (kPair) st_cluster_u32(peer_abort, 1u);  // the peer leaves its loops too
@@ -255,6 +269,10 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
         mbar_init(bar(B_PVFULL), 1);
         mbar_init(bar(B_PVFREE), kPair ? 16 : 256);       // every correction thread / warp of both CTAs
+        if constexpr (kDB) {
+            mbar_init(pv_full(1), 1);
+            mbar_init(pv_free(1), 256);
+        }
         for (int i = 0; i < 8; ++i) mbar_init(bar(B_XM + i), 64);    // both halves of 32 rows
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B_AFULL + i), 128);     // softmax half 0 (writes alpha)
@@ -347,7 +365,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         float ks_next = (half * 64 < lk) ? kscale[half] : 0.f;
         int s3 = 0, s3ph = 0;                               // S/P buffer of tile t and its phase
         const int T_sm = ok ? T : 0;
-        for (int t = 0; t < T_sm; ++t, s3 = (s3 == kNS - 1) ? 0 : s3 + 1, s3ph ^= (s3 == 0) ? 1 : 0) {
+        for (int t = 0; t < T_sm; ++t, s3 = (s3 == kNSb - 1) ? 0 : s3 + 1, s3ph ^= (s3 == 0) ? 1 : 0) {
             const int sb = t & 1;
             const float ks = ks_next;
             const int kb_next = 2 * (t + 1) + half;
@@ -529,7 +547,8 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 for (int e = 0; e < (kB64 ? 2 : 1); ++e) {  // PV epochs of this tile
                     const float alpha = e ? alpha_b : alpha_a;
                     const bool unit = __all_sync(0xffffffffu, alpha == 1.0f);   // RN(RO * 1) == RO
-                    if (!wwait(bar(B_PVFULL), kB64 ? e : (t & 1), abort_flag)) {
+                    const int pj = kDB ? e : 0;                 // PV buffer of this epoch
+                    if (!wwait(pv_full(pj), kDB ? (t & 1) : (kB64 ? e : (t & 1)), abort_flag)) {
                         if (lane == 0) fail(R_CORRECT, t);
                         ok = false;
                         break;
@@ -538,7 +557,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
                     for (int c = 0; c < kDH / 32; ++c) {
                         uint32_t v[16];                         // FP16 tile sums, two per register
-                        tmem_ld32_pack16(tmem + lane_base + TM_PV + half * kDH + c * 32, v);
+                        tmem_ld32_pack16(tmem + lane_base + tm_pv(pj) + half * kDH + c * 32, v);
                         tmem_wait_ld();
                         if (c == kDH / 32 - 1) {
                             tc_fence_before();
@@ -546,7 +565,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                                 __syncwarp();
                                 if (lane == 0) mbar_arrive_cluster(mapa_rank(bar(B_PVFREE), 0));
                             } else {
-                                mbar_arrive(bar(B_PVFREE));
+                                mbar_arrive(pv_free(pj));
                             }
                         }
                         if constexpr (kCkpt) {
@@ -698,7 +717,9 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // whose P the PV MMA issued before it (same thread, in order) reads.
             auto issue_qk = [&](int t) -> bool {
                 if (!bwait(bar(B_KFULL + k_st), k_ph, abort_flag)) return false;
-                if (t >= kNS && !bwait(bar(B_SFREE + qb), qph ^ 1, abort_flag)) return false;
+                // kDB: P-ready of the tile that used this buffer, waited before its
+                // PV, already implies that the softmax has read its S
+                if (!kDB && t >= kNS && !bwait(bar(B_SFREE + qb), qph ^ 1, abort_flag)) return false;
                 tc_fence_after();
                 const uint64_t bK = dK + (uint64_t)(k_st * (kTileKBytes >> 4));
                 const uint32_t dS = tmem + TM_S + qb * 128;
@@ -714,7 +735,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 commit(bar(B_SFULL + qb));
                 commit(bar(B_KEMPTY + k_st));
                 if (++k_st == kNK) { k_st = 0; k_ph ^= 1; }
-                if (++qb == kNS) { qb = 0; qph ^= 1; }
+                if (++qb == kNSb) { qb = 0; qph ^= 1; }
                 return true;
             };
             // The operands that are almost always ready are checked first, so
@@ -727,32 +748,41 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
                 for (int e = 0; e < kEpochs; ++e) {
                     const int n = t * kEpochs + e;                           // PV accumulator use
-                    if (n >= 1 && !bwait(bar(B_PVFREE), (n - 1) & 1, abort_flag)) return false;
+                    const int pj = kDB ? e : 0;
+                    if (kDB ? (t >= 1 && !bwait(pv_free(pj), (t - 1) & 1, abort_flag))
+                            : (n >= 1 && !bwait(bar(B_PVFREE), (n - 1) & 1, abort_flag)))
+                        return false;
                     if (e == 0 && !bwait(bar(B_PFULL + pb), pph, abort_flag)) return false;
                     tc_fence_after();
 #pragma unroll
                     for (int j = 0; j < kSteps; ++j) {
                         const int kk = e * kSteps + j;
                         if constexpr (kPair)
-                            mma2_f8_ts(tmem + TM_PV, aP + kk * 8, bV + (uint64_t)(kk * (32 >> 4)), kIdescPV,
+                            mma2_f8_ts(tmem + tm_pv(pj), aP + kk * 8, bV + (uint64_t)(kk * (32 >> 4)), kIdescPV,
                                        j > 0 ? 1u : 0u);
                         else
-                            mma_f8_ts(tmem + TM_PV, aP + kk * 8, bV + (uint64_t)(kk * (32 >> 4)), kIdescPV,
+                            mma_f8_ts(tmem + tm_pv(pj), aP + kk * 8, bV + (uint64_t)(kk * (32 >> 4)), kIdescPV,
                                       j > 0 ? 1u : 0u);
                     }
-                    commit(bar(B_PVFULL));
+                    commit(pv_full(pj));
                 }
                 commit(bar(B_VEMPTY + v_st));
                 if (++v_st == kNV) { v_st = 0; v_ph ^= 1; }
-                if (++pb == kNS) { pb = 0; pph ^= 1; }
+                if (++pb == kNSb) { pb = 0; pph ^= 1; }
                 return true;
             };
             if (ok) ok = issue_qk(0);
             if (ok && T > 1) ok = issue_qk(1);
             for (int t = 0; t < T && ok; ++t) {
                 fail_tile = t;
-                if (t + 2 < T) ok = issue_qk(t + 2);
-                if (ok && !kCapture) ok = issue_pv(t);
+                if constexpr (kDB) {
+                    // PV(t) first: QK(t+2) reuses the S/P buffer whose P it reads
+                    ok = issue_pv(t);
+                    if (ok && t + 2 < T) ok = issue_qk(t + 2);
+                } else {
+                    if (t + 2 < T) ok = issue_qk(t + 2);
+                    if (ok && !kCapture) ok = issue_pv(t);
+                }
             }
             if (!ok) fail(R_MMA, fail_tile);
             // Drain: all MMAs issued by this thread complete before teardown.
