@@ -40,6 +40,7 @@ CONFIG_ID = 4
 DTYPE = "int8 QK (FP16 integer codes) + e4m3 PV, FP32 accumulate, bf16 in/out"
 FALLBACK_BF16_TFLOPS = 1900.0
 E2E_HEAD_GROUPS = 6     # head ranges of the overlapped host entry (4..8 measured best on this workload)
+E2E_WINDOWS = 3         # end-to-end timing windows (the median is reported)
 
 
 def parse_args():
@@ -365,33 +366,42 @@ def run_e2e(args, w, phys, o_phys, bufs, stream, world, ops, dev):
                                          head_groups=E2E_HEAD_GROUPS, stream=stream)
 
     def timed(fn):
+        """Median over E2E_WINDOWS windows of K back-to-back steps (each window's
+        mean per step, max over ranks).  Host<->device copies on this pool now
+        and then stall for about 20 ms; the median keeps one such stall from
+        deciding the figure, and every window is reported."""
         for _ in range(max(args.warmup, 3)):
             fn()
         torch.cuda.synchronize()
         K = max(1, min(args.steps, 20))
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-        a.record(stream)
-        for _ in range(K):
-            fn()
-        b.record(stream)
-        torch.cuda.synchronize()
-        return max_over_ranks(a.elapsed_time(b) / K, world, dev), K
+        windows = []
+        for _ in range(E2E_WINDOWS):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            if world > 1:
+                dist.barrier()
+            torch.cuda.synchronize()
+            a.record(stream)
+            for _ in range(K):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            windows.append(max_over_ranks(a.elapsed_time(b) / K, world, dev))
+        return sorted(windows)[len(windows) // 2], K, windows
 
-    ms, K = timed(overlapped)
-    ms_seq, _ = timed(sequential)
+    ms, K, win = timed(overlapped)
+    ms_seq, _, win_seq = timed(sequential)
     if S.sage_get_device_status() != S.SAGE_OK:
         raise RuntimeError("device status reports an error after the end-to-end steps")
     h2d = sum(x.numel() * x.element_size() for x in host_in)
     d2h = host_out.numel() * host_out.element_size()
     return {"value": whole_job_tops(ops, world, ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": K,
+            "timing": f"median of {E2E_WINDOWS} windows of {K} back-to-back steps",
+            "window_ms_per_step": [round(x, 4) for x in win],
             "api": (f"sage_attention_host_overlapped (pinned host buffers, {E2E_HEAD_GROUPS} head ranges, "
                     "copies inside the timed region)"),
             "sequential_entry": {"api": "sage_attention_host", "value": whole_job_tops(ops, world, ms_seq),
-                                 "ms_per_step": ms_seq}}
+                                 "ms_per_step": ms_seq, "window_ms_per_step": [round(x, 4) for x in win_seq]}}
 
 
 def run_forms(args):
