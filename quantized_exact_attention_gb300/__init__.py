@@ -9,6 +9,7 @@ is missing, loading it raises.
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 from dataclasses import dataclass
 
@@ -127,8 +128,15 @@ def _check(rc: int, what: str):
         raise SageError(rc, what)
 
 
+# torch's raw current-stream accessor (a handle without a Stream object); the
+# public torch.cuda.current_stream() costs several microseconds per call
+_raw_current_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream_ptr(stream) -> int | None:
     if stream is None:
+        if _raw_current_stream is not None:
+            return _raw_current_stream(torch.cuda.current_device()) or None
         stream = torch.cuda.current_stream()
     return stream.cuda_stream or None
 
@@ -146,9 +154,10 @@ def buffer_sizes(B: int, H: int, Nq: int, Nkv: int, D: int = D_HEAD) -> sage_siz
     return s
 
 
-@dataclass
+@dataclass(frozen=True)
 class PrepBuffers:
-    """Device buffers of sage_prep_buffers, allocated by torch."""
+    """Device buffers of sage_prep_buffers, allocated by torch.  Frozen: the C
+    struct of their addresses is built once and reused by every call."""
     q16: torch.Tensor
     k16: torch.Tensor
     v8t: torch.Tensor
@@ -161,12 +170,16 @@ class PrepBuffers:
     workspace: torch.Tensor
     nkv_pad: int
 
-    def c_struct(self) -> sage_prep_buffers:
+    @functools.cached_property
+    def _c(self) -> sage_prep_buffers:
         ptr = lambda t: t.data_ptr() if t is not None else None  # noqa: E731
         return sage_prep_buffers(ptr(self.q16), ptr(self.k16), ptr(self.v8t), ptr(self.q_scale),
                                  ptr(self.k_scale), ptr(self.v_scale), ptr(self.k_mean),
                                  ptr(self.q8), ptr(self.k8), ptr(self.workspace),
                                  self.workspace.numel())
+
+    def c_struct(self) -> sage_prep_buffers:
+        return self._c
 
 
 def alloc_prep_buffers(B, H, Nq, Nkv, device="cuda", int8_codes=False, D=D_HEAD) -> PrepBuffers:
