@@ -3,10 +3,10 @@ path, each compared with the oracle of the same form.
 
 The cases are drawn once from a fixed seed, so the sweep is the same on
 every run.  Each draws the form (default, causal, one-call entry, BKV = 64,
-D = 64, CTA pairs and their causal variants), batch and head counts, query and
-key lengths (1-384, spanning several tiles and a ragged tail), the physical
-layout (NHD or HND) and, for half the cases, per-item q_len / kv_len between
-0 and the buffer length.  The checks are those of the edge-case tests: the
+D = 64, D = 64 with BKV = 64, CTA pairs and their causal variants), batch
+and head counts, query and key lengths (1-384, spanning several tiles and a
+ragged tail), the physical layout (NHD or HND) and, for half the cases,
+per-item q_len / kv_len between 0 and the buffer length.  The checks are those of the edge-case tests: the
 output within the tolerance, rows that see no key zero, rows past q_len left
 untouched.
 """
@@ -22,7 +22,8 @@ from tests.test_gpu_edges_forms import CANARY, FORMS, _run_form
 
 pytestmark = pytest.mark.gpu
 
-FUZZ_FORMS = {"default": {}, **FORMS, "bkv64_causal": dict(bkv=64, causal=True)}
+FUZZ_FORMS = {"default": {}, **FORMS, "bkv64_causal": dict(bkv=64, causal=True),
+              "d64_bkv64": dict(D=64, bkv=64)}
 
 
 def _draw_cases(n=40, seed=2026):
