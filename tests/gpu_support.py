@@ -64,7 +64,7 @@ class GpuRun:
         torch.cuda.synchronize()
         return self
 
-    def attn(self, fill=None, causal=False, bkv=128):
+    def attn(self, fill=None, causal=False, bkv=128, pairs=False):
         w = self.w
         base = torch.empty((w.B, w.Nq, w.H, w.D), dtype=torch.bfloat16, device="cuda")
         if fill is None:
@@ -72,7 +72,8 @@ class GpuRun:
         else:
             base.fill_(fill)
         self.out = base.permute(0, 2, 1, 3)
-        S.sage_attn_fwd(self.bufs, self.out, self.q_len, self.kv_len, Nkv=w.Nkv, causal=causal, bkv=bkv)
+        S.sage_attn_fwd(self.bufs, self.out, self.q_len, self.kv_len, Nkv=w.Nkv, causal=causal, bkv=bkv,
+                        pairs=pairs)
         torch.cuda.synchronize()
         assert S.sage_get_device_status() == S.SAGE_OK
         return self
@@ -129,6 +130,28 @@ def out_metrics(gpu_bits: np.ndarray, ref_bits: np.ndarray):
     den = float(np.linalg.norm(r))
     rel = float(np.linalg.norm(g - r) / den) if den > 0 else float(np.linalg.norm(g - r))
     return excess, rel, float(diff.max())
+
+
+def literal_bar_audit(gpu_bits: np.ndarray, ref_bits: np.ndarray):
+    """Elements whose |difference| exceeds the literal max-abs 1e-2 bar.
+
+    Returns (count, all_adjacent): all_adjacent is True when every such
+    element is exactly one BF16 step away from the oracle value (neighbouring
+    bit patterns of the same sign) and the oracle value has |o| >= 2, where
+    one BF16 step (>= 2^-6 = 0.0156) is itself larger than 1e-2.
+    """
+    g = O.bf16_bits_to_f32(gpu_bits).astype(np.float64)
+    r = O.bf16_bits_to_f32(ref_bits).astype(np.float64)
+    over = np.abs(g - r) > OUT_MAX_ABS
+    n = int(np.count_nonzero(over))
+    if n == 0:
+        return 0, True
+    gb = gpu_bits[over].astype(np.int32)
+    rb = ref_bits[over].astype(np.int32)
+    same_sign = (gb & 0x8000) == (rb & 0x8000)
+    adjacent = same_sign & (np.abs(gb - rb) == 1)
+    large = np.abs(r[over]) >= 2.0
+    return n, bool(np.all(adjacent & large))
 
 
 def within_tolerance(gpu_bits, ref_bits):

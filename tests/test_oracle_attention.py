@@ -66,6 +66,34 @@ def test_oracle_close_to_fp64_attention(cfg):
     assert rel <= 5e-2
 
 
+def test_oracle_ragged_workload_close_to_fp64_attention():
+    # the ragged-tail workload (two batch items, 1000 and 777 tokens, 16
+    # heads, K channel offsets): every valid row of every head
+    w = W.make_config(3)
+    q, k, v = _logical(w)
+    prep = O.prepare(q, k, v, w.q_len, w.kv_len)
+    out = O.bf16_bits_to_f32(O.attention(prep))
+    for b, (lq, lk) in enumerate(zip(w.qlens, w.kvlens)):
+        ref = fp64_attention(q[b:b + 1, :, :lq], k[b:b + 1, :, :lk], v[b:b + 1, :, :lk])
+        cos, rel = _metrics(out[b:b + 1, :, :lq], ref)
+        assert cos >= 0.999 and rel <= 5e-2, (b, cos, rel)
+
+
+def test_oracle_long_sequence_close_to_fp64_attention():
+    # the 16K-token workload on sampled rows: two heads, 128 rows from the
+    # first, a middle and the last query tile, each against all 16384 keys
+    w = W.make_config(4)
+    q, k, v = _logical(w)
+    rows = np.concatenate([np.arange(0, 32), np.arange(8192, 8224), np.arange(16384 - 64, 16384)])
+    for h in (0, 17):
+        qh, kh, vh = q[:, h:h + 1], k[:, h:h + 1], v[:, h:h + 1]
+        prep = O.prepare(qh, kh, vh)
+        got, _ = O.attention_rows(prep, 0, 0, rows)
+        ref = fp64_attention(qh[:, :, rows], kh, vh)
+        cos, rel = _metrics(O.bf16_bits_to_f32(got)[None, None], ref)
+        assert cos >= 0.999 and rel <= 5e-2, (h, cos, rel)
+
+
 def test_oracle_varlen_close_to_fp64_attention():
     w = W.make_custom(B=2, H=2, Nq=300, Nkv=300, seed=21, k_offset_std=2.0,
                       q_len=[300, 211], kv_len=[300, 157])
