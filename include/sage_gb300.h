@@ -97,7 +97,9 @@ typedef struct {
 int sage_buffer_sizes(int B, int H, int Nq, int Nkv, int D, sage_sizes* out);
 
 /* Preparation (Experiment Log, "Phase 0 Import And Verification": Q/K
- * preparation, K smoothing, INT8 quantization, FP8 V).
+ * preparation, K smoothing, INT8 quantization, FP8 V).  Three kernel
+ * launches: K/V channel statistics with the Q quantization, the per-head
+ * finalize, and the K/V quantization.
  *  q, k, v : BF16 inputs [B,H,Nq,D], [B,H,Nkv,D], [B,H,Nkv,D] (device).
  *  q_len, kv_len : device int32 [B] valid lengths (<= Nq, <= Nkv), or NULL
  *                  for all rows valid.  Out-of-range lengths are clamped.
@@ -105,7 +107,9 @@ int sage_buffer_sizes(int B, int H, int Nq, int Nkv, int D, sage_sizes* out);
  * Steps: per (b,h,channel) mean of the valid keys in a fixed order (chunks of
  * 64 tokens summed in order, chunk sums in order, one division); K - mean;
  * per-block amax, scale = amax/127, codes rne(x*127/amax); V per channel to
- * e4m3 with scale amax/1.125.  Enqueues three kernels. */
+ * e4m3 with scale amax/1.125.  Calls on the same workspace must be ordered
+ * (one stream, or events): the workspace holds the call's statistics and its
+ * synchronisation words. */
 int sage_prep_qkv(const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
                   int B, int H, int Nq, int Nkv, int D,
                   const int32_t* q_len, const int32_t* kv_len,
@@ -233,15 +237,19 @@ int sage_attention_host(const sage_copy* inputs, int n_inputs,
                         const sage_copy* output,
                         int B, int H, int Nq, int Nkv, int D, float sm_scale, void* stream);
 
-/* Launch form of sage_attn_fwd and sage_attn_fwd_causal (process-wide;
- * returns the previous setting).  1: adjacent query tiles run as clusters of
+/* The CTA-pair launch form of sage_attn_fwd (causal = 0) and
+ * sage_attn_fwd_causal (causal = 1): adjacent query tiles run as clusters of
  * two CTAs sharing each tensor-core instruction (tcgen05 .cta_group::2, 256
- * rows), each CTA loading half of every K and V tile.  0 (default): one CTA
- * per 128-row query tile.  Both forms compute the same values in the same
- * order (bit-identical outputs); the other entry points always use the
- * one-CTA form.  On GB300 the paired form is slower for this kernel: every
- * tile's PV waits for P-ready arrivals from both CTAs, which cross SMs. */
-int sage_set_cta_pairing(int enable);
+ * rows), each CTA loading half of every K and V tile.  Both forms compute the
+ * same values in the same order, so the output is bit-identical to the
+ * one-CTA form's.  Arguments, layouts and errors as for sage_attn_fwd.  On
+ * GB300 the paired form is slower for this kernel (every tile's PV waits for
+ * P-ready arrivals from both CTAs, which cross SMs); the other entry points
+ * always use one CTA per 128-row query tile. */
+int sage_attn_fwd_pairs(const sage_prep_buffers* in, const sage_tensor* o,
+                        int B, int H, int Nq, int Nkv, int D,
+                        const int32_t* q_len, const int32_t* kv_len,
+                        float sm_scale, int causal, void* stream);
 
 /* End-to-end call from host memory with the copies overlapped with the
  * compute.  The heads of a problem are independent (K mean, quantization
@@ -291,7 +299,10 @@ int sage_last_launch_count(void);
  * memory pool is fully committed.  This entry point takes the same arguments
  * and fills the same outputs bit for bit, but ignores out->workspace and uses
  * a fixed 16 MiB device array inside the library instead, which every GPU that
- * loads the library holds until the process exits.
+ * loads the library holds until the process exits.  Its V codes and scales
+ * are those of the default BKV = 128 contract (|v| <= 1.125): pair it with
+ * sage_attn_fwd, sage_attn_fwd_causal or sage_attn_fwd_bkv(bkv = 128), not
+ * with the BKV = 64 form, whose V scaling differs.
  *  - Allocates nothing (no cudaMalloc/cudaFree, no allocating library call).
  *  - The first call on a device looks up that device's address of the array
  *    (cudaGetSymbolAddress); make that first call before any stream capture.
@@ -316,6 +327,16 @@ size_t sage_prep_noalloc_capacity(void);
  * tensor memory and returns; mode 0 restores normal launches.  Use only on
  * a problem of one or a few query tiles (each CTA waits about one second). */
 int sage_debug_inject_fault(int mode);
+
+/* Test hook for the preparation tests and measurements (process-wide; not
+ * for production use): one_pass = 1 makes later preparation calls use a
+ * single launch that reads K and V from HBM once (a work queue in which each
+ * head's K/V quantization trails its channel statistics, re-reading K and V
+ * from L2) instead of the default three launches (statistics and Q,
+ * finalize, K/V quantization); both compute the same bytes, and the single
+ * launch is the slower of the two on GB300.  lag > 0 fixes how many heads the
+ * K/V items trail their statistics (0: chosen from the grid size). */
+int sage_debug_prep_mode(int one_pass, int lag);
 
 #ifdef __cplusplus
 }

@@ -31,11 +31,11 @@ HEAD_DIMS = (64, 128)       # head dimensions the kernels are built for
 
 # Names the header declares (checked by the CPU tests against the .so exports).
 EXPORTED = ("sage_buffer_sizes", "sage_prep_qkv", "sage_attn_fwd", "sage_attn_fwd_causal", "sage_attention",
-            "sage_attn_checkpoints", "sage_prep_qkv_bkv", "sage_attn_fwd_bkv", "sage_set_cta_pairing",
+            "sage_attn_checkpoints", "sage_prep_qkv_bkv", "sage_attn_fwd_bkv", "sage_attn_fwd_pairs",
             "sage_attention_host_overlapped",
             "sage_qk_int32",
             "sage_attention_host", "sage_get_device_status", "sage_status_string",
-            "sage_last_launch_count", "sage_debug_inject_fault", "sage_prep_qkv_noalloc",
+            "sage_last_launch_count", "sage_debug_inject_fault", "sage_debug_prep_mode", "sage_prep_qkv_noalloc",
             "sage_prep_noalloc_capacity")
 
 
@@ -106,7 +106,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sage_status_string.restype = ctypes.c_char_p
     lib.sage_last_launch_count.argtypes = []
     lib.sage_debug_inject_fault.argtypes = [i]
-    lib.sage_set_cta_pairing.argtypes = [i]
+    lib.sage_debug_prep_mode.argtypes = [i, i]
+    lib.sage_debug_prep_mode.restype = ctypes.c_int
+    lib.sage_attn_fwd_pairs.argtypes = [P(sage_prep_buffers), P(sage_tensor), i, i, i, i, i, vp, vp, f, i, vp]
     lib.sage_attention_host_overlapped.argtypes = [P(sage_tensor)] * 8 + [i, i, i, i, i, f, i, i,
                                                                           P(sage_prep_buffers), vp]
     lib.sage_prep_qkv_noalloc.argtypes = lib.sage_prep_qkv.argtypes
@@ -237,14 +239,22 @@ def sage_prep_noalloc_capacity() -> int:
 
 
 def sage_attn_fwd(bufs: PrepBuffers, o, q_len=None, kv_len=None, sm_scale: float = 0.0, stream=None,
-                  Nkv: int | None = None, causal: bool = False, bkv: int = 128):
+                  Nkv: int | None = None, causal: bool = False, bkv: int = 128, pairs: bool = False):
     """Enqueue the fused attention kernel; o is a [B,H,Nq,D] BF16 view.
     causal=True calls sage_attn_fwd_causal (key j visible to query i iff
-    j <= i + kv_len - q_len); bkv = 64 calls sage_attn_fwd_bkv."""
+    j <= i + kv_len - q_len); bkv = 64 calls sage_attn_fwd_bkv; pairs=True
+    calls sage_attn_fwd_pairs (the CTA-pair launch form)."""
     B, H, Nq, D = o.shape
     Nkv = bufs.k16.shape[2] if Nkv is None else Nkv
     os_, pb = tensor_desc(o), bufs.c_struct()
     lib = load_library()
+    if pairs:
+        if bkv != 128:
+            raise ValueError("the CTA-pair form serves the BKV = 128 contract only")
+        rc = lib.sage_attn_fwd_pairs(ctypes.byref(pb), ctypes.byref(os_), B, H, Nq, Nkv, D, _lens(q_len),
+                                     _lens(kv_len), float(sm_scale), 1 if causal else 0, _stream_ptr(stream))
+        _check(rc, "sage_attn_fwd_pairs")
+        return
     if bkv != 128:
         rc = lib.sage_attn_fwd_bkv(ctypes.byref(pb), ctypes.byref(os_), B, H, Nq, Nkv, D, _lens(q_len),
                                    _lens(kv_len), float(sm_scale), int(bkv), 1 if causal else 0,
@@ -348,13 +358,14 @@ def sage_last_launch_count() -> int:
     return int(load_library().sage_last_launch_count())
 
 
-def sage_set_cta_pairing(enable: bool) -> bool:
-    """Select the CTA-pair form of sage_attn_fwd[_causal]; returns the previous setting."""
-    return bool(load_library().sage_set_cta_pairing(1 if enable else 0))
-
-
 def sage_debug_inject_fault(mode: int):
     _check(load_library().sage_debug_inject_fault(int(mode)), "sage_debug_inject_fault")
+
+
+def sage_debug_prep_mode(one_pass: bool = False, lag: int = 0):
+    """Test hook: select the one-launch preparation (one_pass=True, queue lag
+    `lag` heads, 0 = from the grid) or the default three launches for later calls."""
+    _check(load_library().sage_debug_prep_mode(1 if one_pass else 0, int(lag)), "sage_debug_prep_mode")
 
 
 def attention(q, k, v, q_len=None, kv_len=None, sm_scale: float = 0.0, out=None, int8_codes=False,

@@ -105,7 +105,8 @@ int check_prep_buffers(const sage_prep_buffers* p, bool need_workspace, const sa
 int status_from(cudaError_t e) { return e == cudaSuccess ? SAGE_OK : SAGE_ERR_LAUNCH; }
 
 int fault_mode_for_next_launch = 0;
-int g_cta_pairing = 0;          // sage_set_cta_pairing (pairs measured slower; off by default)
+int g_prep_one_pass = 0;        // sage_debug_prep_mode: 1 = the one-launch preparation
+int g_prep_lag = 0;             // sage_debug_prep_mode: one-pass queue lag (0 = from the grid)
 
 }  // namespace
 
@@ -120,6 +121,8 @@ int* device_status_ptr() {
     }
     return g_status_ptr[dev];
 }
+
+void set_last_launch_count(int n) { g_last_launches = n; }
 
 }  // namespace sage
 
@@ -143,8 +146,9 @@ int sage_buffer_sizes(int B, int H, int Nq, int Nkv, int D, sage_sizes* out) {
     out->k_mean = (size_t)(bh * D * 4);
     out->q8 = (size_t)(bh * Nq * D);
     out->k8 = (size_t)(bh * Nkv * D);
-    // partial sums + partial amax [B,H,chunks,D] and the V inverse scales [B,H,D]
-    out->workspace = (size_t)(2 * bh * nchunks * D * 4 + bh * D * 4);
+    // partial sums + partial amax [B,H,chunks,D], the V inverse scales [B,H,D]
+    // and 16 bytes of synchronisation words per head
+    out->workspace = prep_workspace_bytes(bh, nchunks, D);
     out->nkv_pad = pad;
     return SAGE_OK;
 }
@@ -177,13 +181,11 @@ static int prep_common(const sage_tensor* q, const sage_tensor* k, const sage_te
     p.q16 = out->q16; p.k16 = out->k16; p.v8t = out->v8t;
     p.q8 = out->q8; p.k8 = out->k8;
     p.q_scale = out->q_scale; p.k_scale = out->k_scale; p.v_scale = out->v_scale; p.k_mean = out->k_mean;
-    float* ws = static_cast<float*>(out->workspace);
-    const int64_t part = (int64_t)B * H * p.n_chunks * D;
-    p.psum = ws;
-    p.pamax = ws + part;
-    p.v_inv = ws + 2 * part;
+    set_prep_workspace(p, out->workspace);
+    p.status = device_status_ptr();
+    p.prep_lag = g_prep_lag;
     int launches = 0;
-    rc = status_from(launch_prep(p, true, static_cast<cudaStream_t>(stream), &launches));
+    rc = status_from(launch_prep(p, true, static_cast<cudaStream_t>(stream), &launches, g_prep_one_pass != 0));
     if (rc == SAGE_OK) g_last_launches = launches;
     return rc;
 }
@@ -208,7 +210,7 @@ int sage_prep_qkv_bkv(const sage_tensor* q, const sage_tensor* k, const sage_ten
 static int attn_common(const sage_prep_buffers* in, const sage_tensor* o, int32_t* s_out, int B, int H, int Nq,
                        int Nkv, int D, const int32_t* q_len, const int32_t* kv_len, float sm_scale,
                        void* stream, bool capture, bool causal, const CkptParams* ck = nullptr,
-                       bool bkv64 = false, int h_begin = 0, int h_count = -1) {
+                       bool bkv64 = false, int h_begin = 0, int h_count = -1, bool pairs = false) {
     int rc = check_shape(B, H, Nq, Nkv, D);
     if (rc != SAGE_OK) return rc;
     sage_sizes sz;
@@ -225,7 +227,7 @@ static int attn_common(const sage_prep_buffers* in, const sage_tensor* o, int32_
     const uint64_t bh = (uint64_t)B * H;
     // CTA pairs serve the default and causal forms; each CTA of a pair loads
     // half of every K tile (64 keys) and of every V tile (D/2 channels)
-    const bool pair = g_cta_pairing != 0 && !capture && ck == nullptr && !bkv64;
+    const bool pair = pairs && !capture && ck == nullptr && !bkv64;
     CUtensorMap tq, tk, tv;
     // Q/K code images: boxes of 64 channels (128 bytes, one swizzle row) x 128
     // rows (K: 64 rows when paired); V^T: boxes of 128 tokens x D (D/2) channels.
@@ -280,6 +282,12 @@ int sage_attn_fwd(const sage_prep_buffers* in, const sage_tensor* o, int B, int 
 int sage_attn_fwd_causal(const sage_prep_buffers* in, const sage_tensor* o, int B, int H, int Nq, int Nkv, int D,
                          const int32_t* q_len, const int32_t* kv_len, float sm_scale, void* stream) {
     return attn_common(in, o, nullptr, B, H, Nq, Nkv, D, q_len, kv_len, sm_scale, stream, false, true);
+}
+
+int sage_attn_fwd_pairs(const sage_prep_buffers* in, const sage_tensor* o, int B, int H, int Nq, int Nkv, int D,
+                        const int32_t* q_len, const int32_t* kv_len, float sm_scale, int causal, void* stream) {
+    return attn_common(in, o, nullptr, B, H, Nq, Nkv, D, q_len, kv_len, sm_scale, stream, false, causal != 0,
+                       nullptr, false, 0, -1, true);
 }
 
 int sage_attn_fwd_bkv(const sage_prep_buffers* in, const sage_tensor* o, int B, int H, int Nq, int Nkv, int D,
@@ -348,13 +356,11 @@ int sage_attention(const sage_tensor* q, const sage_tensor* k, const sage_tensor
     pp.q_len = q_len; pp.kv_len = kv_len;
     pp.k16 = buf->k16; pp.v8t = buf->v8t; pp.k8 = buf->k8;
     pp.k_scale = buf->k_scale; pp.v_scale = buf->v_scale; pp.k_mean = buf->k_mean;
-    float* ws = static_cast<float*>(buf->workspace);
-    const int64_t part = (int64_t)B * H * pp.n_chunks * D;
-    pp.psum = ws;
-    pp.pamax = ws + part;
-    pp.v_inv = ws + 2 * part;
+    set_prep_workspace(pp, buf->workspace);
+    pp.status = status;
+    pp.prep_lag = g_prep_lag;
     int prep_launches = 0;
-    if ((rc = status_from(launch_prep(pp, false, s, &prep_launches))) != SAGE_OK) return rc;
+    if ((rc = status_from(launch_prep(pp, false, s, &prep_launches, g_prep_one_pass != 0))) != SAGE_OK) return rc;
 
     // attention with the Q quantization in its prologue
     const uint64_t bh = (uint64_t)B * H, d = (uint64_t)D;
@@ -543,16 +549,19 @@ const char* sage_status_string(int code) {
 
 int sage_last_launch_count(void) { return g_last_launches; }
 
-int sage_set_cta_pairing(int enable) {
-    const int old = g_cta_pairing;
-    g_cta_pairing = enable != 0;
-    return old;
-}
-
 // Test hook (not part of the public header): the next sage_attn_fwd launch
 // withholds one V tile copy so its consumer's bounded wait runs out.
 int sage_debug_inject_fault(int mode) {
     fault_mode_for_next_launch = mode;
+    return SAGE_OK;
+}
+
+// Test hook: preparation form for later calls (process-wide, tests only).
+// one_pass = 1 selects the single launch that reads K and V once instead of
+// the three plain launches; lag > 0 fixes its queue lag in heads.
+int sage_debug_prep_mode(int one_pass, int lag) {
+    g_prep_one_pass = one_pass != 0;
+    g_prep_lag = lag > 0 ? lag : 0;
     return SAGE_OK;
 }
 

@@ -42,8 +42,33 @@ struct PrepParams {
     float* psum;                           // workspace [B,H,n_chunks,D]
     float* pamax;                          // workspace [B,H,n_chunks,D]
     float* v_inv;                          // workspace [B,H,D]
+    unsigned long long* stats_done;        // workspace [B,H]: (launch epoch << 32) | finished statistics items
+    uint32_t* ready;                       // workspace [B,H]: launch epoch once the head's statistics are final
+    int* queue;                            // workspace [H]: one-pass work counter of the range starting at head h
+    int* status;                           // device status words (a bounded wait that ran out)
+    int prep_lag;                          // one-pass queue lag in heads; <= 0: chosen from the grid
     float sv;                              // target |v| of the V codes: 144 / BKV (1.125 or 2.25)
 };
+
+// Workspace bytes: chunk sums and maxima [B,H,chunks,D], V inverse scales
+// [B,H,D] (floats), then the one-pass synchronisation words (12 B per head)
+// and work counters (4 B per head), 16 B per head in all.
+inline size_t prep_workspace_bytes(int64_t bh, int64_t nchunks, int64_t D) {
+    return (size_t)(2 * bh * nchunks * D * 4 + bh * D * 4 + bh * 16);
+}
+// Point the workspace fields of p (whose B, H, D and n_chunks are set) at a
+// workspace of that size.
+inline void set_prep_workspace(PrepParams& p, void* ws) {
+    const int64_t bh = (int64_t)p.B * p.H;
+    float* f = static_cast<float*>(ws);
+    const int64_t part = bh * p.n_chunks * p.D;
+    p.psum = f;
+    p.pamax = f + part;
+    p.v_inv = f + 2 * part;
+    p.stats_done = reinterpret_cast<unsigned long long*>(f + 2 * part + bh * p.D);
+    p.ready = reinterpret_cast<uint32_t*>(p.stats_done + bh);
+    p.queue = reinterpret_cast<int*>(p.ready + bh);
+}
 
 // Stage checkpoints of one query tile (see sage_attn_checkpoints).
 struct CkptParams {
@@ -80,10 +105,13 @@ struct AttnParams {
 constexpr int kStatusWords = 4;
 
 int* device_status_ptr();                  // per-device address of the status words
+void set_last_launch_count(int n);         // what sage_last_launch_count() reports next
 
 // with_q = false: K/V statistics and quantization only (Q is quantized by the
 // attention kernel of the fused entry point).
-cudaError_t launch_prep(const PrepParams& p, bool with_q, cudaStream_t s, int* launches);
+// one_pass: the single launch that reads K and V once, instead of the three
+// plain launches (same bytes; measured slower on GB300).
+cudaError_t launch_prep(const PrepParams& p, bool with_q, cudaStream_t s, int* launches, bool one_pass = false);
 // Which form of the attention kernel to launch.
 struct AttnMode {
     bool capture = false;   // QK checkpoint only (int32 scores)

@@ -101,11 +101,10 @@ extern "C" int sage_prep_qkv_noalloc(const sage_tensor* q, const sage_tensor* k,
     p.q16 = out->q16; p.k16 = out->k16; p.v8t = out->v8t;
     p.q8 = out->q8; p.k8 = out->k8;
     p.q_scale = out->q_scale; p.k_scale = out->k_scale; p.v_scale = out->v_scale; p.k_mean = out->k_mean;
-    const int64_t part = (int64_t)B * H * p.n_chunks * D;
-    p.psum = scratch;
-    p.pamax = scratch + part;
-    p.v_inv = scratch + 2 * part;
+    set_prep_workspace(p, scratch);
+    p.status = device_status_ptr();
     int launches = 0;
-    return launch_prep(p, true, static_cast<cudaStream_t>(stream), &launches) == cudaSuccess ? SAGE_OK
-                                                                                         : SAGE_ERR_LAUNCH;
+    if (launch_prep(p, true, static_cast<cudaStream_t>(stream), &launches) != cudaSuccess) return SAGE_ERR_LAUNCH;
+    set_last_launch_count(launches);
+    return SAGE_OK;
 }

@@ -404,18 +404,6 @@ __device__ __forceinline__ void add_f16x2_to(float& a0, float& a1, uint32_t h2) 
         : "+f"(a0), "+f"(a1) : "r"(h2));
 }
 
-// Per-warpgroup register budget change; every warp of the warpgroup must
-// execute the same instruction.  The sum over warpgroups must stay within the
-// registers the block was launched with, or an increase waits forever.
-template <uint32_t N>
-__device__ __forceinline__ void setmaxnreg_inc() {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <uint32_t N>
-__device__ __forceinline__ void setmaxnreg_dec() {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

@@ -49,10 +49,11 @@ def test_buffer_sizes(lib):
     assert s.k16 == 2 * 16 * 777 * 128 * 2
     assert s.v8t == 2 * 16 * 128 * 784
     assert s.q_scale == 2 * 16 * 8 * 4 and s.k_scale == 2 * 16 * 13 * 4
-    assert s.workspace == 2 * (2 * 16 * 13 * 128 * 4) + 2 * 16 * 128 * 4
+    # chunk sums and maxima, V inverse scales, 16 B of one-pass words per head
+    assert s.workspace == 2 * (2 * 16 * 13 * 128 * 4) + 2 * 16 * 128 * 4 + 2 * 16 * 16
     s64 = S.buffer_sizes(2, 16, 1000, 777, D=64)
     assert s64.q16 == 2 * 16 * 1000 * 64 * 2 and s64.v8t == 2 * 16 * 64 * 784
-    assert s64.workspace == 2 * (2 * 16 * 13 * 64 * 4) + 2 * 16 * 64 * 4
+    assert s64.workspace == 2 * (2 * 16 * 13 * 64 * 4) + 2 * 16 * 64 * 4 + 2 * 16 * 16
 
 
 @pytest.mark.parametrize("shape,code", [((0, 1, 1, 1, 128), S.SAGE_ERR_ARG),

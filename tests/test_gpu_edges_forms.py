@@ -49,12 +49,9 @@ def _run_form(w, form):
     if form.get("fused"):
         S.sage_attention(run.q, run.k, run.v, out, run.bufs, run.q_len, run.kv_len, causal=causal)
     else:
-        old = S.sage_set_cta_pairing(form.get("pairs", False))
-        try:
-            run.prep(bkv=bkv)
-            S.sage_attn_fwd(run.bufs, out, run.q_len, run.kv_len, Nkv=w.Nkv, causal=causal, bkv=bkv)
-        finally:
-            S.sage_set_cta_pairing(old)
+        run.prep(bkv=bkv)
+        S.sage_attn_fwd(run.bufs, out, run.q_len, run.kv_len, Nkv=w.Nkv, causal=causal, bkv=bkv,
+                        pairs=form.get("pairs", False))
     torch.cuda.synchronize()
     assert S.sage_get_device_status() == S.SAGE_OK
     return out.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)

@@ -28,11 +28,7 @@ CASES = {
 
 
 def _run(w, causal, pairing):
-    old = S.sage_set_cta_pairing(pairing)
-    try:
-        return G.GpuRun(w).prep().attn(fill=9.0, causal=causal).out_bits()
-    finally:
-        S.sage_set_cta_pairing(old)
+    return G.GpuRun(w).prep().attn(fill=9.0, causal=causal, pairs=pairing).out_bits()
 
 
 @pytest.mark.parametrize("name", sorted(CASES))

@@ -9,6 +9,7 @@ preparation test here uses), on consecutive calls that reuse the array with
 different shapes.  This file is named so pytest collects it last.
 """
 import ctypes
+import dataclasses
 
 import pytest
 import torch
@@ -24,7 +25,7 @@ def _prep_both(w):
     run = G.GpuRun(w, int8_codes=True)                        # regular entry point, own workspace
     run.prep()
     ref = {f: getattr(run.bufs, f).clone() for f in FIELDS}
-    nb = S.alloc_prep_buffers(w.B, w.H, w.Nq, w.Nkv, "cuda", int8_codes=True)
+    nb = S.alloc_prep_buffers(w.B, w.H, w.Nq, w.Nkv, "cuda", int8_codes=True, D=w.D)
     for f in FIELDS:                                          # poison the outputs first
         getattr(nb, f).fill_(0x5A if getattr(nb, f).dtype in (torch.uint8, torch.int8) else 7)
     S.sage_prep_qkv_noalloc(run.q, run.k, run.v, nb, run.q_len, run.kv_len)
@@ -46,9 +47,33 @@ def test_noalloc_prep_matches_regular_prep_on_two_calls_in_a_row():
     first = W.make_config(3)                                  # varlen, 2 x 16 heads of 1000 tokens
     second = W.make_custom(B=1, H=24, Nq=2048, Nkv=3000, seed=31, layout="hnd",
                            k_offset_std=2.0)
-    for w in (first, second):
+    third = W.make_custom(B=2, H=6, Nq=500, Nkv=1300, D=64, seed=34, layout="hnd",   # D = 64, varlen
+                          k_offset_std=2.0, q_len=[500, 77], kv_len=[1300, 640])
+    for w in (first, second, third):
         ref, nb = _prep_both(w)
         _assert_equal(ref, nb)
+
+
+@pytest.mark.gpu
+def test_noalloc_prep_ignores_the_callers_workspace():
+    # a NULL workspace of 0 bytes is accepted, and a poisoned workspace passed
+    # in is left untouched: the scratch is the library's own array
+    G.ensure_built()
+    w = W.make_custom(B=2, H=8, Nq=700, Nkv=900, D=64, seed=33, layout="hnd", k_offset_std=2.0,
+                      q_len=[700, 333], kv_len=[900, 401])
+    run = G.GpuRun(w, int8_codes=True)
+    run.prep()
+    ref = {f: getattr(run.bufs, f).clone() for f in FIELDS}
+    for workspace in (torch.empty(0, dtype=torch.uint8, device="cuda"),
+                      torch.full_like(run.bufs.workspace, 0xA5)):
+        nb = S.alloc_prep_buffers(w.B, w.H, w.Nq, w.Nkv, "cuda", int8_codes=True, D=64)
+        nb = dataclasses.replace(nb, workspace=workspace)
+        S.sage_prep_qkv_noalloc(run.q, run.k, run.v, nb, run.q_len, run.kv_len)
+        torch.cuda.synchronize()
+        assert S.sage_get_device_status() == S.SAGE_OK
+        assert S.sage_last_launch_count() == 3          # the three preparation kernels
+        _assert_equal(ref, nb)
+        assert workspace.numel() == 0 or bool((workspace == 0xA5).all())
 
 
 @pytest.mark.gpu
