@@ -69,7 +69,9 @@ typedef struct {
  *   v_scale f32  [B, H, D]          per channel
  *   k_mean  f32  [B, H, D]          channel mean removed from K
  *   q8, k8  int8 [B, H, Nq|Nkv, D]  optional INT8 code bytes (NULL: skipped)
- *   workspace                       scratch of sage_buffer_sizes().workspace
+ *   workspace                       scratch of sage_buffer_sizes().workspace (its last
+ *                                   8*B bytes, rounded up to 16, are the lengths slot of
+ *                                   the host-memory entries)
  * Rows at or beyond a batch item's valid length are written as code 0 and
  * scales of blocks holding no valid row are 0, so no uninitialised byte is
  * ever read by sage_attn_fwd. */
@@ -230,12 +232,19 @@ typedef struct {
 /* End-to-end call from host memory: copies every `inputs` region host->device,
  * runs sage_prep_qkv and sage_attn_fwd on the device views q, k, v, o (which
  * point into those regions), then copies `output` device->host, all on
- * `stream`, without synchronizing.  Lengths are taken as all-valid. */
+ * `stream`, without synchronizing.
+ *  q_len, kv_len : HOST int32 [B] valid lengths (clamped to [0, Nq] and
+ *                  [0, Nkv]), or NULL for all rows valid.  They are copied
+ *                  into the lengths slot at the end of buf->workspace before
+ *                  the call returns, so the arrays may be reused at once.
+ *                  Rows >= q_len[b] of the device output are not written;
+ *                  the `output` region is copied back as given. */
 int sage_attention_host(const sage_copy* inputs, int n_inputs,
                         const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
                         const sage_prep_buffers* buf, const sage_tensor* o,
                         const sage_copy* output,
-                        int B, int H, int Nq, int Nkv, int D, float sm_scale, void* stream);
+                        int B, int H, int Nq, int Nkv, int D,
+                        const int32_t* q_len, const int32_t* kv_len, float sm_scale, void* stream);
 
 /* The CTA-pair launch form of sage_attn_fwd (causal = 0) and
  * sage_attn_fwd_causal (causal = 1): adjacent query tiles run as clusters of
@@ -265,8 +274,12 @@ int sage_attn_fwd_pairs(const sage_prep_buffers* in, const sage_tensor* o,
  *            rows of a head, are contiguous.
  *  causal  : 0 or 1 as for sage_attention.
  *  head_groups : 1 .. H.
+ *  q_len, kv_len : HOST int32 [B] valid lengths, or NULL for all valid, as
+ *            for sage_attention_host; only rows [0, q_len[b]) of Q and O and
+ *            [0, kv_len[b]) of K and V are copied, so host output rows at or
+ *            beyond q_len[b] are left untouched.
  *  buf     : full-size buffers as for sage_prep_qkv (each range uses its own
- *            heads' slices).  Lengths are taken as all valid.
+ *            heads' slices).
  * The work is ordered after prior work on `stream` and later work on
  * `stream` waits for all of it; the call does not synchronize.  The internal
  * streams and events are created on the first call on a device and kept.
@@ -277,6 +290,7 @@ int sage_attention_host_overlapped(const sage_tensor* q_host, const sage_tensor*
                                    const sage_tensor* v_host, const sage_tensor* o_host,
                                    const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
                                    const sage_tensor* o, int B, int H, int Nq, int Nkv, int D,
+                                   const int32_t* q_len, const int32_t* kv_len,
                                    float sm_scale, int causal, int head_groups,
                                    const sage_prep_buffers* buf, void* stream);
 
@@ -337,6 +351,16 @@ int sage_debug_inject_fault(int mode);
  * launch is the slower of the two on GB300.  lag > 0 fixes how many heads the
  * K/V items trail their statistics (0: chosen from the grid size). */
 int sage_debug_prep_mode(int one_pass, int lag);
+
+/* Test hook for the attention tests and measurements (process-wide; not for
+ * production use): tma_store = 1 makes later sage_attn_fwd and
+ * sage_attn_fwd_causal launches (the other forms are unaffected) write each
+ * output tile whose rows are all valid through a TMA store of the BF16 tile
+ * staged in shared memory (a partial tile of a shorter batch item is still
+ * written row by row); 0 (default) writes every row with per-thread 16-byte
+ * stores.  Both write the same bytes; the TMA form is the slower one on
+ * GB300. */
+int sage_debug_epilogue_mode(int tma_store);
 
 #ifdef __cplusplus
 }

@@ -35,7 +35,8 @@ EXPORTED = ("sage_buffer_sizes", "sage_prep_qkv", "sage_attn_fwd", "sage_attn_fw
             "sage_attention_host_overlapped",
             "sage_qk_int32",
             "sage_attention_host", "sage_get_device_status", "sage_status_string",
-            "sage_last_launch_count", "sage_debug_inject_fault", "sage_debug_prep_mode", "sage_prep_qkv_noalloc",
+            "sage_last_launch_count", "sage_debug_inject_fault", "sage_debug_prep_mode",
+            "sage_debug_epilogue_mode", "sage_prep_qkv_noalloc",
             "sage_prep_noalloc_capacity")
 
 
@@ -100,16 +101,17 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sage_qk_int32.argtypes = [P(sage_prep_buffers), vp, i, i, i, i, i, vp, vp, vp]
     lib.sage_attention_host.argtypes = [P(sage_copy), i, P(sage_tensor), P(sage_tensor), P(sage_tensor),
                                         P(sage_prep_buffers), P(sage_tensor), P(sage_copy),
-                                        i, i, i, i, i, f, vp]
+                                        i, i, i, i, i, vp, vp, f, vp]
     lib.sage_get_device_status.argtypes = []
     lib.sage_status_string.argtypes = [i]
     lib.sage_status_string.restype = ctypes.c_char_p
     lib.sage_last_launch_count.argtypes = []
     lib.sage_debug_inject_fault.argtypes = [i]
     lib.sage_debug_prep_mode.argtypes = [i, i]
+    lib.sage_debug_epilogue_mode.argtypes = [i]
     lib.sage_debug_prep_mode.restype = ctypes.c_int
     lib.sage_attn_fwd_pairs.argtypes = [P(sage_prep_buffers), P(sage_tensor), i, i, i, i, i, vp, vp, f, i, vp]
-    lib.sage_attention_host_overlapped.argtypes = [P(sage_tensor)] * 8 + [i, i, i, i, i, f, i, i,
+    lib.sage_attention_host_overlapped.argtypes = [P(sage_tensor)] * 8 + [i, i, i, i, i, vp, vp, f, i, i,
                                                                           P(sage_prep_buffers), vp]
     lib.sage_prep_qkv_noalloc.argtypes = lib.sage_prep_qkv.argtypes
     lib.sage_prep_noalloc_capacity.argtypes = []
@@ -311,14 +313,25 @@ def sage_qk_int32(bufs: PrepBuffers, s: torch.Tensor, q_len=None, kv_len=None, s
     _check(rc, "sage_qk_int32")
 
 
+def _host_lens(x, B):
+    """A host int32 [B] array for the host-memory entries (None stays None)."""
+    if x is None:
+        return None
+    vals = [int(v) for v in (x.tolist() if hasattr(x, "tolist") else x)]
+    if len(vals) != B:
+        raise ValueError(f"expected {B} lengths")
+    return (ctypes.c_int32 * B)(*vals)
+
+
 def sage_attention_host(host_phys, dev_phys, views_of, bufs: PrepBuffers, o_dev, o_host,
-                        sm_scale: float = 0.0, stream=None):
+                        sm_scale: float = 0.0, stream=None, q_len=None, kv_len=None):
     """End-to-end call: copy host buffers in, prep + attention, copy O out.
 
     host_phys / dev_phys: matching lists of pinned-host / device tensors
     holding the physical inputs; views_of(dev_phys) -> (q, k, v) [B,H,N,D]
     views; o_dev / o_host: device output view and its pinned host twin
-    (same physical layout, contiguous).
+    (same physical layout, contiguous); q_len / kv_len: per-item lengths as
+    host sequences (None: all valid).
     """
     q, k, v = views_of(dev_phys)
     B, H, Nq, D = q.shape
@@ -330,21 +343,24 @@ def sage_attention_host(host_phys, dev_phys, views_of, bufs: PrepBuffers, o_dev,
     qs, ks, vs, os_, pb = tensor_desc(q), tensor_desc(k), tensor_desc(v), tensor_desc(o_dev), bufs.c_struct()
     rc = load_library().sage_attention_host(copies, n, ctypes.byref(qs), ctypes.byref(ks), ctypes.byref(vs),
                                             ctypes.byref(pb), ctypes.byref(os_), ctypes.byref(out),
-                                            B, H, Nq, Nkv, D, float(sm_scale), _stream_ptr(stream))
+                                            B, H, Nq, Nkv, D, _host_lens(q_len, B), _host_lens(kv_len, B),
+                                            float(sm_scale), _stream_ptr(stream))
     _check(rc, "sage_attention_host")
 
 
 def sage_attention_host_overlapped(q_host, k_host, v_host, o_host, q, k, v, o, bufs: PrepBuffers,
                                    sm_scale: float = 0.0, causal: bool = False, head_groups: int = 4,
-                                   stream=None):
+                                   stream=None, q_len=None, kv_len=None):
     """End-to-end call with copies overlapped with compute: host views
     q_host.. (pinned, same strides as the device views q..), per head range
-    copy in, prep, attention, copy out."""
+    copy in, prep, attention, copy out; q_len / kv_len: per-item lengths as
+    host sequences (None: all valid; only valid rows are copied)."""
     B, H, Nq, D = q.shape
     Nkv = k.shape[2]
     descs = [tensor_desc(t) for t in (q_host, k_host, v_host, o_host, q, k, v, o)]
     pb = bufs.c_struct()
     rc = load_library().sage_attention_host_overlapped(*[ctypes.byref(d) for d in descs], B, H, Nq, Nkv, D,
+                                                       _host_lens(q_len, B), _host_lens(kv_len, B),
                                                        float(sm_scale), 1 if causal else 0, int(head_groups),
                                                        ctypes.byref(pb), _stream_ptr(stream))
     _check(rc, "sage_attention_host_overlapped")
@@ -360,6 +376,12 @@ def sage_last_launch_count() -> int:
 
 def sage_debug_inject_fault(mode: int):
     _check(load_library().sage_debug_inject_fault(int(mode)), "sage_debug_inject_fault")
+
+
+def sage_debug_epilogue_mode(tma_store: bool = False):
+    """Test hook: write full output tiles through a TMA store (True) or row by
+    row (False, the default) in later attention launches."""
+    _check(load_library().sage_debug_epilogue_mode(1 if tma_store else 0), "sage_debug_epilogue_mode")
 
 
 def sage_debug_prep_mode(one_pass: bool = False, lag: int = 0):

@@ -5,6 +5,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "sage_gb300.h"
 #include "sage_internal.h"
@@ -107,6 +108,7 @@ int status_from(cudaError_t e) { return e == cudaSuccess ? SAGE_OK : SAGE_ERR_LA
 int fault_mode_for_next_launch = 0;
 int g_prep_one_pass = 0;        // sage_debug_prep_mode: 1 = the one-launch preparation
 int g_prep_lag = 0;             // sage_debug_prep_mode: one-pass queue lag (0 = from the grid)
+int g_tma_epilogue = 0;         // sage_debug_epilogue_mode: 1 = TMA-store epilogue
 
 }  // namespace
 
@@ -148,7 +150,7 @@ int sage_buffer_sizes(int B, int H, int Nq, int Nkv, int D, sage_sizes* out) {
     out->k8 = (size_t)(bh * Nkv * D);
     // partial sums + partial amax [B,H,chunks,D], the V inverse scales [B,H,D]
     // and 16 bytes of synchronisation words per head
-    out->workspace = prep_workspace_bytes(bh, nchunks, D);
+    out->workspace = prep_workspace_bytes(B, H, nchunks, D);
     out->nkv_pad = pad;
     return SAGE_OK;
 }
@@ -228,9 +230,10 @@ static int attn_common(const sage_prep_buffers* in, const sage_tensor* o, int32_
     // CTA pairs serve the default and causal forms; each CTA of a pair loads
     // half of every K tile (64 keys) and of every V tile (D/2 channels)
     const bool pair = pairs && !capture && ck == nullptr && !bkv64;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     // Q/K code images: boxes of 64 channels (128 bytes, one swizzle row) x 128
-    // rows (K: 64 rows when paired); V^T: boxes of 128 tokens x D (D/2) channels.
+    // rows (K: 64 rows when paired); V^T: boxes of 128 tokens x D (D/2) channels;
+    // O (the TMA-store epilogue): boxes of 64 channels x 128 rows.
     const uint64_t d = (uint64_t)D;
     if (!encode_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, in->q16, d, (uint64_t)Nq, bh, d * 2,
                    (uint64_t)Nq * d * 2, 64, 128) ||
@@ -238,6 +241,11 @@ static int attn_common(const sage_prep_buffers* in, const sage_tensor* o, int32_
                    (uint64_t)Nkv * d * 2, 64, pair ? 64 : 128) ||
         !encode_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, in->v8t, (uint64_t)sz.nkv_pad, d, bh,
                    (uint64_t)sz.nkv_pad, (uint64_t)sz.nkv_pad * d, 128, (uint32_t)(pair ? D / 2 : D)))
+        return encode_fn() ? SAGE_ERR_UNSUPPORTED : SAGE_ERR_DRIVER;
+    if (capture)
+        to = tq;                                           // no output
+    else if (!encode_bf16_view(&to, o->ptr, d, (uint64_t)Nq, (uint64_t)H, (uint64_t)B, o->stride_n, o->stride_h,
+                               o->stride_b))
         return encode_fn() ? SAGE_ERR_UNSUPPORTED : SAGE_ERR_DRIVER;
 
     AttnParams p{};
@@ -256,11 +264,12 @@ static int attn_common(const sage_prep_buffers* in, const sage_tensor* o, int32_
     p.c = (float)(scale * (1.0 / std::log(2.0)));
     p.status = status;
     p.fault_mode = fault_mode_for_next_launch;
+    p.tma_out = g_tma_epilogue;
     fault_mode_for_next_launch = 0;
     int launches = 0;
     if (ck != nullptr) {
         p.ck = *ck;
-        rc = status_from(launch_attn_checkpoints(p, tq, tk, tv, causal, static_cast<cudaStream_t>(stream)));
+        rc = status_from(launch_attn_checkpoints(p, tq, tk, tv, to, causal, static_cast<cudaStream_t>(stream)));
         launches = 1;
     } else {
         AttnMode mode;
@@ -268,7 +277,7 @@ static int attn_common(const sage_prep_buffers* in, const sage_tensor* o, int32_
         mode.causal = causal;
         mode.bkv64 = bkv64;
         mode.pair = pair;
-        rc = status_from(launch_attn(p, tq, tk, tv, mode, static_cast<cudaStream_t>(stream), &launches));
+        rc = status_from(launch_attn(p, tq, tk, tv, to, mode, static_cast<cudaStream_t>(stream), &launches));
     }
     if (rc == SAGE_OK) g_last_launches = launches;
     return rc;
@@ -364,9 +373,11 @@ int sage_attention(const sage_tensor* q, const sage_tensor* k, const sage_tensor
 
     // attention with the Q quantization in its prologue
     const uint64_t bh = (uint64_t)B * H, d = (uint64_t)D;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     if (!encode_bf16_view(&tq, q->ptr, d, (uint64_t)Nq, (uint64_t)H, (uint64_t)B, q->stride_n, q->stride_h,
                           q->stride_b) ||
+        !encode_bf16_view(&to, o->ptr, d, (uint64_t)Nq, (uint64_t)H, (uint64_t)B, o->stride_n, o->stride_h,
+                          o->stride_b) ||
         !encode_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, buf->k16, d, (uint64_t)Nkv, bh, d * 2,
                    (uint64_t)Nkv * d * 2, 64, 128) ||
         !encode_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, buf->v8t, (uint64_t)sz.nkv_pad, d, bh,
@@ -385,34 +396,67 @@ int sage_attention(const sage_tensor* q, const sage_tensor* k, const sage_tensor
     p.c = (float)(scale * (1.0 / std::log(2.0)));
     p.status = status;
     p.fault_mode = fault_mode_for_next_launch;
+    p.tma_out = g_tma_epilogue;
     fault_mode_for_next_launch = 0;
     int launches = 0;
     AttnMode mode;
     mode.causal = causal != 0;
     mode.fused_q = true;
-    rc = status_from(launch_attn(p, tq, tk, tv, mode, s, &launches));
+    rc = status_from(launch_attn(p, tq, tk, tv, to, mode, s, &launches));
     if (rc == SAGE_OK) g_last_launches = launches + prep_launches;
     return rc;
 }
 
+// Host-memory entries: stage per-item lengths given as host arrays (NULL:
+// all valid; values clamped to [0, n]) into the workspace's lengths slot on
+// `s`.  Fills the clamped values into lq/lk (host) and points *q_dev/*kv_dev
+// at the device copies (NULL when the host array was NULL).
+static int stage_host_lens(const sage_prep_buffers* buf, int B, int H, int Nq, int Nkv, int D,
+                           const int32_t* q_len, const int32_t* kv_len, cudaStream_t s, int32_t* lq,
+                           int32_t* lk, const int32_t** q_dev, const int32_t** kv_dev) {
+    for (int b = 0; b < B; ++b) {
+        lq[b] = q_len ? (q_len[b] < 0 ? 0 : (q_len[b] > Nq ? Nq : q_len[b])) : Nq;
+        lk[b] = kv_len ? (kv_len[b] < 0 ? 0 : (kv_len[b] > Nkv ? Nkv : kv_len[b])) : Nkv;
+    }
+    *q_dev = *kv_dev = nullptr;
+    if (q_len == nullptr && kv_len == nullptr) return SAGE_OK;
+    if (buf == nullptr || buf->workspace == nullptr) return SAGE_ERR_ARG;
+    sage_sizes sz;
+    sage_buffer_sizes(B, H, Nq, Nkv, D, &sz);
+    if (buf->workspace_bytes < sz.workspace) return SAGE_ERR_ARG;
+    int32_t* slot = prep_lens_slot(buf->workspace, B, H, ceil_div(Nkv, kMeanChunk), D);
+    // pageable sources: the copies are staged before cudaMemcpyAsync returns
+    if (cudaMemcpyAsync(slot, lq, sizeof(int32_t) * B, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(slot + B, lk, sizeof(int32_t) * B, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return SAGE_ERR_LAUNCH;
+    if (q_len) *q_dev = slot;
+    if (kv_len) *kv_dev = slot + B;
+    return SAGE_OK;
+}
+
 int sage_attention_host(const sage_copy* inputs, int n_inputs, const sage_tensor* q, const sage_tensor* k,
                         const sage_tensor* v, const sage_prep_buffers* buf, const sage_tensor* o,
-                        const sage_copy* output, int B, int H, int Nq, int Nkv, int D, float sm_scale,
-                        void* stream) {
+                        const sage_copy* output, int B, int H, int Nq, int Nkv, int D,
+                        const int32_t* q_len, const int32_t* kv_len, float sm_scale, void* stream) {
     if (inputs == nullptr || n_inputs <= 0 || output == nullptr) return SAGE_ERR_ARG;
     int rc = check_shape(B, H, Nq, Nkv, D);
     if (rc != SAGE_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    std::vector<int32_t> lq(B), lk(B);
+    const int32_t *q_dev = nullptr, *kv_dev = nullptr;
+    if ((rc = stage_host_lens(buf, B, H, Nq, Nkv, D, q_len, kv_len, s, lq.data(), lk.data(), &q_dev, &kv_dev)) !=
+        SAGE_OK)
+        return rc;
     for (int i = 0; i < n_inputs; ++i) {
         if (!inputs[i].host || !inputs[i].device) return SAGE_ERR_ARG;
         if (cudaMemcpyAsync(inputs[i].device, inputs[i].host, inputs[i].bytes, cudaMemcpyHostToDevice, s) !=
             cudaSuccess)
             return SAGE_ERR_LAUNCH;
     }
-    rc = sage_prep_qkv(q, k, v, B, H, Nq, Nkv, D, nullptr, nullptr, buf, stream);
+    rc = sage_prep_qkv(q, k, v, B, H, Nq, Nkv, D, q_dev, kv_dev, buf, stream);
     if (rc != SAGE_OK) return rc;
     const int prep_launches = g_last_launches;
-    rc = sage_attn_fwd(buf, o, B, H, Nq, Nkv, D, nullptr, nullptr, sm_scale, stream);
+    rc = sage_attn_fwd(buf, o, B, H, Nq, Nkv, D, q_dev, kv_dev, sm_scale, stream);
     if (rc != SAGE_OK) return rc;
     g_last_launches += prep_launches;
     if (!output->host || !output->device) return SAGE_ERR_ARG;
@@ -422,19 +466,22 @@ int sage_attention_host(const sage_copy* inputs, int n_inputs, const sage_tensor
     return SAGE_OK;
 }
 
-// Copy heads [h0, h0 + nh) of a [B, H, N, D] BF16 tensor (element strides of
-// t; the same physical layout on both sides) with 2-D copies.
-static int copy_heads(void* dst, const void* src, const sage_tensor* t, int B, int N, int D, int h0, int nh,
-                      cudaMemcpyKind kind, cudaStream_t s) {
+// Copy rows [0, rows[b]) of heads [h0, h0 + nh) of a [B, H, N, D] BF16 tensor
+// (element strides of t; the same physical layout on both sides) with 2-D
+// copies.
+static int copy_heads(void* dst, const void* src, const sage_tensor* t, int B, const int32_t* rows, int D, int h0,
+                      int nh, cudaMemcpyKind kind, cudaStream_t s) {
     const int64_t sb = t->stride_b, sh = t->stride_h, sn = t->stride_n;
     for (int b = 0; b < B; ++b) {
+        const int N = rows[b];
+        if (N <= 0) continue;
         const int64_t off = (b * sb + (int64_t)h0 * sh) * 2;
         char* d = static_cast<char*>(dst) + off;
         const char* c = static_cast<const char*>(src) + off;
         cudaError_t e;
         if (sh == D && sn >= (int64_t)nh * D)          // a row holds the head range contiguously
             e = cudaMemcpy2DAsync(d, sn * 2, c, sn * 2, (size_t)nh * D * 2, (size_t)N, kind, s);
-        else if (sn == D && sh >= (int64_t)N * D)      // each head is one contiguous block
+        else if (sn == D && sh >= (int64_t)N * D)      // each head's valid rows are one contiguous block
             e = cudaMemcpy2DAsync(d, sh * 2, c, sh * 2, (size_t)N * D * 2, (size_t)nh, kind, s);
         else {
             e = cudaSuccess;
@@ -474,8 +521,8 @@ static OverlapStreams* overlap_streams() {
 int sage_attention_host_overlapped(const sage_tensor* q_host, const sage_tensor* k_host, const sage_tensor* v_host,
                                    const sage_tensor* o_host, const sage_tensor* q, const sage_tensor* k,
                                    const sage_tensor* v, const sage_tensor* o, int B, int H, int Nq, int Nkv, int D,
-                                   float sm_scale, int causal, int head_groups, const sage_prep_buffers* buf,
-                                   void* stream) {
+                                   const int32_t* q_len, const int32_t* kv_len, float sm_scale, int causal,
+                                   int head_groups, const sage_prep_buffers* buf, void* stream) {
     int rc = check_shape(B, H, Nq, Nkv, D);
     if (rc != SAGE_OK) return rc;
     if (head_groups < 1 || head_groups > H) return SAGE_ERR_ARG;
@@ -491,6 +538,11 @@ int sage_attention_host_overlapped(const sage_tensor* q_host, const sage_tensor*
     OverlapStreams* os = overlap_streams();
     if (os == nullptr) return SAGE_ERR_LAUNCH;
     cudaStream_t user = static_cast<cudaStream_t>(stream);
+    std::vector<int32_t> lq(B), lk(B);
+    const int32_t *q_dev = nullptr, *kv_dev = nullptr;
+    if ((rc = stage_host_lens(buf, B, H, Nq, Nkv, D, q_len, kv_len, user, lq.data(), lk.data(), &q_dev, &kv_dev)) !=
+        SAGE_OK)
+        return rc;
     if (cudaEventRecord(os->start, user) != cudaSuccess) return SAGE_ERR_LAUNCH;
     for (int i = 0; i < 3; ++i)
         if (cudaStreamWaitEvent(os->s[i], os->start, 0) != cudaSuccess) return SAGE_ERR_LAUNCH;
@@ -498,21 +550,22 @@ int sage_attention_host_overlapped(const sage_tensor* q_host, const sage_tensor*
     for (int g = 0; g < head_groups && rc == SAGE_OK; ++g) {
         const int h0 = (int)((int64_t)H * g / head_groups), h1 = (int)((int64_t)H * (g + 1) / head_groups);
         cudaStream_t s = os->s[g % 3];
-        if ((rc = copy_heads(const_cast<void*>(q->ptr), q_host->ptr, q, B, Nq, D, h0, h1 - h0,
+        if ((rc = copy_heads(const_cast<void*>(q->ptr), q_host->ptr, q, B, lq.data(), D, h0, h1 - h0,
                              cudaMemcpyHostToDevice, s)) != SAGE_OK ||
-            (rc = copy_heads(const_cast<void*>(k->ptr), k_host->ptr, k, B, Nkv, D, h0, h1 - h0,
+            (rc = copy_heads(const_cast<void*>(k->ptr), k_host->ptr, k, B, lk.data(), D, h0, h1 - h0,
                              cudaMemcpyHostToDevice, s)) != SAGE_OK ||
-            (rc = copy_heads(const_cast<void*>(v->ptr), v_host->ptr, v, B, Nkv, D, h0, h1 - h0,
+            (rc = copy_heads(const_cast<void*>(v->ptr), v_host->ptr, v, B, lk.data(), D, h0, h1 - h0,
                              cudaMemcpyHostToDevice, s)) != SAGE_OK)
             break;
-        rc = prep_common(q, k, v, B, H, Nq, Nkv, D, nullptr, nullptr, kSV, buf, s, h0, h1 - h0);
+        rc = prep_common(q, k, v, B, H, Nq, Nkv, D, q_dev, kv_dev, kSV, buf, s, h0, h1 - h0);
         if (rc != SAGE_OK) break;
         launches += g_last_launches;
-        rc = attn_common(buf, o, nullptr, B, H, Nq, Nkv, D, nullptr, nullptr, sm_scale, s, false, causal != 0,
+        rc = attn_common(buf, o, nullptr, B, H, Nq, Nkv, D, q_dev, kv_dev, sm_scale, s, false, causal != 0,
                          nullptr, false, h0, h1 - h0);
         if (rc != SAGE_OK) break;
         launches += g_last_launches;
-        rc = copy_heads(const_cast<void*>(o_host->ptr), o->ptr, o, B, Nq, D, h0, h1 - h0, cudaMemcpyDeviceToHost, s);
+        rc = copy_heads(const_cast<void*>(o_host->ptr), o->ptr, o, B, lq.data(), D, h0, h1 - h0,
+                        cudaMemcpyDeviceToHost, s);
     }
     // the caller's stream resumes after every group, also on an error
     for (int i = 0; i < 3; ++i) {
@@ -559,6 +612,11 @@ int sage_debug_inject_fault(int mode) {
 // Test hook: preparation form for later calls (process-wide, tests only).
 // one_pass = 1 selects the single launch that reads K and V once instead of
 // the three plain launches; lag > 0 fixes its queue lag in heads.
+int sage_debug_epilogue_mode(int tma_store) {
+    g_tma_epilogue = tma_store != 0;
+    return SAGE_OK;
+}
+
 int sage_debug_prep_mode(int one_pass, int lag) {
     g_prep_one_pass = one_pass != 0;
     g_prep_lag = lag > 0 ? lag : 0;

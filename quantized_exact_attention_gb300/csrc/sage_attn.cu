@@ -160,10 +160,11 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
 // barriers; rank 0's commits arrive on both CTAs' barriers; the P-ready and
 // PV-consumed arrivals of both CTAs' warps go to rank 0.
 template <int D, bool kCapture, bool kCausal, bool kFusedQ, bool kCkpt = false, bool kB64 = false,
-          bool kPair = false>
+          bool kPair = false, bool kTmaOut = false>
 __global__ void __launch_bounds__(kThreads, 1)
 sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                 const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                 const AttnParams p) {
     static_assert(!kPair || (!kCapture && !kFusedQ && !kCkpt && !kB64), "paired CTAs: default and causal forms");
     using L = Smem<D, kPair>;
     constexpr uint32_t kKBlock = L::kKBlock;
@@ -296,6 +297,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         if (!kCapture) tma_prefetch_desc(&tm_v);
+        if (kTmaOut) tma_prefetch_desc(&tm_o);
     }
     tc_fence_before();
     __syncthreads();
@@ -591,6 +593,16 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     for (int i = 0; i < kDH / 4; ++i) dp[i] = make_float4(ro[4 * i], ro[4 * i + 1], ro[4 * i + 2], ro[4 * i + 3]);
                 }
             }
+            // Two epilogue forms, the same bytes.  Default: each thread writes
+            // its row's channels with 16-byte stores.  kTmaOut (a separate
+            // instantiation of the default and causal forms): a tile whose 128
+            // rows are all valid (or valid up to Nq, where the tensor map
+            // clips) is staged in shared memory and leaves through one TMA
+            // store; a partial tile of a shorter batch item is still written
+            // row by row, so rows >= q_len are never touched.  The TMA form
+            // measured slower on GB300: the CTA waits for the store to read
+            // shared memory before it can exit.
+            const bool tma_out = kTmaOut && ((q0 + 128 <= lq) || (lq == p.Nq));
             if (ok && wwait(bar(B_LFULL), 0, abort_flag)) {
                 // l carries the 448 scale of P, so (RO / l) * v_scale is the output
                 const float l_row = l_s[row] + l_s[128 + row];
@@ -598,7 +610,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 const float rl = (kCausal && l_row == 0.f) ? 0.f : __frcp_rn(l_row);
                 if (kCkpt && half == 0) p.ck.recip[row] = rl;
                 const int r = q0 + row;
-                if (r < lq) {
+                if (tma_out || r < lq) {
                     uint4* dst = reinterpret_cast<uint4*>(p.o + b * p.osb + h * p.osh + (int64_t)r * p.osn +
                                                           half * kDH);
 #pragma unroll
@@ -612,11 +624,35 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                             const __nv_bfloat162 pr = __floats2bfloat162_rn(o0, o1);
                             w[j] = *reinterpret_cast<const uint32_t*>(&pr);
                         }
-                        dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+                        if (tma_out) {
+                            // channel c = half*kDH + 8i sits in 64-channel box c/64, 16-byte
+                            // chunk (c%64)/8 of its 128-byte row, XOR-swizzled by row % 8;
+                            // the K ring is free: every MMA has completed
+                            const int c = half * kDH + i * 8;
+                            const uint32_t off = (uint32_t)(c / 64) * kHalfBytes + (uint32_t)row * 128u +
+                                                 ((uint32_t)(((c % 64) / 8) ^ (row & 7)) << 4);
+                            *reinterpret_cast<uint4*>(sgen + OFF_K + off) = make_uint4(w[0], w[1], w[2], w[3]);
+                        } else {
+                            dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
                     }
                 }
+                if (tma_out) fence_proxy_async_smem();      // staged rows visible to the TMA
             } else if (ok) {
                 if (lane == 0) fail(R_CORRECT, T);
+            }
+            // Every correction thread reaches this barrier (each wait above is
+            // bounded; tma_out is uniform over the CTA); the store is issued
+            // only when no role has failed.
+            if constexpr (kTmaOut) {
+                if (tma_out) named_bar_sync(7, 256);
+                if (tma_out && threadIdx.x == 256 && *abort_flag == 0) {
+#pragma unroll
+                    for (int hh = 0; hh < D / 64; ++hh)
+                        tma_store_4d(&tm_o, sbase + OFF_K + hh * kHalfBytes, hh * 64, q0, h, b);
+                    tma_store_commit();
+                    tma_store_wait_read();                  // shared memory read before the CTA exits
+                }
             }
         }
     } else if (warp == kWarpProducer) {
@@ -808,29 +844,31 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
 }
 
-template <int D, bool kCapture, bool kCausal, bool kFusedQ = false, bool kCkpt = false, bool kB64 = false>
+template <int D, bool kCapture, bool kCausal, bool kFusedQ = false, bool kCkpt = false, bool kB64 = false,
+          bool kTmaOut = false>
 cudaError_t launch_one(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, cudaStream_t s) {
+                       const CUtensorMap& tv, const CUtensorMap& to, cudaStream_t s) {
     static bool attr_set[64] = {};                          // per device, per instantiation
     constexpr uint32_t kSmemBytes = Smem<D>::kSmemBytes;
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(sage_attn_kernel<D, kCapture, kCausal, kFusedQ, kCkpt, kB64>,
+        cudaError_t e = cudaFuncSetAttribute(sage_attn_kernel<D, kCapture, kCausal, kFusedQ, kCkpt, kB64, false, kTmaOut>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
     const dim3 grid = kCkpt ? dim3(1, 1, 1) : dim3((unsigned)((p.Nq + 127) / 128), (unsigned)p.h_count, (unsigned)p.B);
-    sage_attn_kernel<D, kCapture, kCausal, kFusedQ, kCkpt, kB64><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+    sage_attn_kernel<D, kCapture, kCausal, kFusedQ, kCkpt, kB64, false, kTmaOut>
+        <<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, to, p);
     return cudaGetLastError();
 }
 
 // Paired form: clusters of two CTAs over an even number of query tiles.
 template <int D, bool kCausal>
 cudaError_t launch_pair(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                        cudaStream_t s) {
+                        const CUtensorMap& to, cudaStream_t s) {
     static bool attr_set[64] = {};
     constexpr uint32_t kSmemBytes = Smem<D, true>::kSmemBytes;
     auto kernel = sage_attn_kernel<D, false, kCausal, false, false, false, true>;
@@ -855,47 +893,51 @@ cudaError_t launch_pair(const AttnParams& p, const CUtensorMap& tq, const CUtens
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, to, p);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_d(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                     const AttnMode& m, cudaStream_t s) {
+                     const CUtensorMap& to, const AttnMode& m, cudaStream_t s) {
     if (m.pair) {
         if (m.capture || m.fused_q || m.bkv64) return cudaErrorInvalidValue;
-        return m.causal ? launch_pair<D, true>(p, tq, tk, tv, s) : launch_pair<D, false>(p, tq, tk, tv, s);
+        return m.causal ? launch_pair<D, true>(p, tq, tk, tv, to, s) : launch_pair<D, false>(p, tq, tk, tv, to, s);
     }
-    if (m.capture) return launch_one<D, true, false>(p, tq, tk, tv, s);   // S does not depend on BKV
+    if (m.capture) return launch_one<D, true, false>(p, tq, tk, tv, to, s);   // S does not depend on BKV
     if (m.bkv64) {
         if (m.fused_q) return cudaErrorInvalidValue;
-        return m.causal ? launch_one<D, false, true, false, false, true>(p, tq, tk, tv, s)
-                        : launch_one<D, false, false, false, false, true>(p, tq, tk, tv, s);
+        return m.causal ? launch_one<D, false, true, false, false, true>(p, tq, tk, tv, to, s)
+                        : launch_one<D, false, false, false, false, true>(p, tq, tk, tv, to, s);
     }
     if (m.fused_q)
-        return m.causal ? launch_one<D, false, true, true>(p, tq, tk, tv, s)
-                        : launch_one<D, false, false, true>(p, tq, tk, tv, s);
-    return m.causal ? launch_one<D, false, true>(p, tq, tk, tv, s) : launch_one<D, false, false>(p, tq, tk, tv, s);
+        return m.causal ? launch_one<D, false, true, true>(p, tq, tk, tv, to, s)
+                        : launch_one<D, false, false, true>(p, tq, tk, tv, to, s);
+    if (p.tma_out)                                          // the TMA-store epilogue form
+        return m.causal ? launch_one<D, false, true, false, false, false, true>(p, tq, tk, tv, to, s)
+                        : launch_one<D, false, false, false, false, false, true>(p, tq, tk, tv, to, s);
+    return m.causal ? launch_one<D, false, true>(p, tq, tk, tv, to, s) : launch_one<D, false, false>(p, tq, tk, tv, to, s);
 }
 
 }  // namespace
 
 cudaError_t launch_attn(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                        const CUtensorMap& tv, const AttnMode& mode, cudaStream_t s, int* launches) {
+                        const CUtensorMap& tv, const CUtensorMap& to, const AttnMode& mode, cudaStream_t s,
+                        int* launches) {
     *launches = 1;
-    if (p.D == 128) return launch_d<128>(p, tq, tk, tv, mode, s);
-    if (p.D == 64) return launch_d<64>(p, tq, tk, tv, mode, s);
+    if (p.D == 128) return launch_d<128>(p, tq, tk, tv, to, mode, s);
+    if (p.D == 64) return launch_d<64>(p, tq, tk, tv, to, mode, s);
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_attn_checkpoints(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                                    const CUtensorMap& tv, bool causal, cudaStream_t s) {
+                                    const CUtensorMap& tv, const CUtensorMap& to, bool causal, cudaStream_t s) {
     if (p.D == 128)
-        return causal ? launch_one<128, false, true, false, true>(p, tq, tk, tv, s)
-                      : launch_one<128, false, false, false, true>(p, tq, tk, tv, s);
+        return causal ? launch_one<128, false, true, false, true>(p, tq, tk, tv, to, s)
+                      : launch_one<128, false, false, false, true>(p, tq, tk, tv, to, s);
     if (p.D == 64)
-        return causal ? launch_one<64, false, true, false, true>(p, tq, tk, tv, s)
-                      : launch_one<64, false, false, false, true>(p, tq, tk, tv, s);
+        return causal ? launch_one<64, false, true, false, true>(p, tq, tk, tv, to, s)
+                      : launch_one<64, false, false, false, true>(p, tq, tk, tv, to, s);
     return cudaErrorInvalidValue;
 }
 

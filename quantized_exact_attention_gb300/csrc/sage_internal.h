@@ -52,9 +52,18 @@ struct PrepParams {
 
 // Workspace bytes: chunk sums and maxima [B,H,chunks,D], V inverse scales
 // [B,H,D] (floats), then the one-pass synchronisation words (12 B per head)
-// and work counters (4 B per head), 16 B per head in all.
-inline size_t prep_workspace_bytes(int64_t bh, int64_t nchunks, int64_t D) {
+// and work counters (4 B per head), 16 B per head in all, then a slot for the
+// per-item lengths [2][B] int32 that the host-memory entries stage there
+// (rounded up to 16 B).
+inline size_t prep_workspace_core(int64_t bh, int64_t nchunks, int64_t D) {
     return (size_t)(2 * bh * nchunks * D * 4 + bh * D * 4 + bh * 16);
+}
+inline size_t prep_workspace_bytes(int64_t B, int64_t H, int64_t nchunks, int64_t D) {
+    return prep_workspace_core(B * H, nchunks, D) + (size_t)((8 * B + 15) / 16) * 16;
+}
+// The lengths slot: q_len at [0, B), kv_len at [B, 2B).
+inline int32_t* prep_lens_slot(void* ws, int64_t B, int64_t H, int64_t nchunks, int64_t D) {
+    return reinterpret_cast<int32_t*>(static_cast<char*>(ws) + prep_workspace_core(B * H, nchunks, D));
 }
 // Point the workspace fields of p (whose B, H, D and n_chunks are set) at a
 // workspace of that size.
@@ -97,6 +106,7 @@ struct AttnParams {
     float c;                               // fp32(sm_scale * log2(e))
     int* status;                           // device status words
     int fault_mode;                        // test hook: 0 = none
+    int tma_out;                           // 1: full output tiles leave through a TMA store (measured slower)
     float* q_scale_out;                    // fused Q only: per-block Q scales written by the kernel
     CkptParams ck;                         // checkpoint kernel only
 };
@@ -121,11 +131,14 @@ struct AttnMode {
     bool pair = false;      // clusters of two CTAs sharing M = 256 MMAs (default and causal forms);
                             // tk / tv then map half tiles (64 keys; D/2 channels)
 };
+// to maps the BF16 output view (box 64 channels x 128 rows, 128-byte
+// swizzle) for the TMA-store epilogue; unused by the capture form.
 cudaError_t launch_attn(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                        const CUtensorMap& tv, const AttnMode& mode, cudaStream_t s, int* launches);
+                        const CUtensorMap& tv, const CUtensorMap& to, const AttnMode& mode, cudaStream_t s,
+                        int* launches);
 // One CTA (p.ck.b, p.ck.h, p.ck.qtile) of the attention kernel, writing its
 // stage checkpoints besides its output rows.
 cudaError_t launch_attn_checkpoints(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                                    const CUtensorMap& tv, bool causal, cudaStream_t s);
+                                    const CUtensorMap& tv, const CUtensorMap& to, bool causal, cudaStream_t s);
 
 }  // namespace sage

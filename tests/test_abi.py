@@ -49,11 +49,12 @@ def test_buffer_sizes(lib):
     assert s.k16 == 2 * 16 * 777 * 128 * 2
     assert s.v8t == 2 * 16 * 128 * 784
     assert s.q_scale == 2 * 16 * 8 * 4 and s.k_scale == 2 * 16 * 13 * 4
-    # chunk sums and maxima, V inverse scales, 16 B of one-pass words per head
-    assert s.workspace == 2 * (2 * 16 * 13 * 128 * 4) + 2 * 16 * 128 * 4 + 2 * 16 * 16
+    # chunk sums and maxima, V inverse scales, 16 B of one-pass words per head,
+    # the host entries' lengths slot (2 x B int32, rounded up to 16 B)
+    assert s.workspace == 2 * (2 * 16 * 13 * 128 * 4) + 2 * 16 * 128 * 4 + 2 * 16 * 16 + 16
     s64 = S.buffer_sizes(2, 16, 1000, 777, D=64)
     assert s64.q16 == 2 * 16 * 1000 * 64 * 2 and s64.v8t == 2 * 16 * 64 * 784
-    assert s64.workspace == 2 * (2 * 16 * 13 * 64 * 4) + 2 * 16 * 64 * 4 + 2 * 16 * 16
+    assert s64.workspace == 2 * (2 * 16 * 13 * 64 * 4) + 2 * 16 * 64 * 4 + 2 * 16 * 16 + 16
 
 
 @pytest.mark.parametrize("shape,code", [((0, 1, 1, 1, 128), S.SAGE_ERR_ARG),
@@ -104,8 +105,8 @@ def test_attn_rejects_bad_arguments_before_touching_the_gpu(lib):
     assert lib.sage_attn_fwd(ctypes.byref(b), None, 1, 1, 128, 128, 128, None, None, 0.0,
                              None) == S.SAGE_ERR_ARG
     assert lib.sage_qk_int32(ctypes.byref(b), None, 1, 1, 128, 128, 128, None, None, None) == S.SAGE_ERR_ARG
-    assert lib.sage_attention_host(None, 0, None, None, None, None, None, None, 1, 1, 1, 1, 128, 0.0,
-                                   None) == S.SAGE_ERR_ARG
+    assert lib.sage_attention_host(None, 0, None, None, None, None, None, None, 1, 1, 1, 1, 128, None, None,
+                                   0.0, None) == S.SAGE_ERR_ARG
 
 
 def test_fused_entry_and_causal_reject_bad_arguments_before_touching_the_gpu(lib):
@@ -137,8 +138,8 @@ def test_overlapped_host_entry_rejects_bad_arguments_before_touching_the_gpu(lib
 
     def call(hq=t, dq=t, groups=4, shape=(1, 8, 256, 256, 128)):
         tens = [hq, t, t, t, dq, t, t, t]
-        return lib.sage_attention_host_overlapped(*[ctypes.byref(x) for x in tens], *shape, 0.0, 0, groups,
-                                                  ctypes.byref(b), None)
+        return lib.sage_attention_host_overlapped(*[ctypes.byref(x) for x in tens], *shape, None, None, 0.0, 0,
+                                                  groups, ctypes.byref(b), None)
 
     assert call(groups=0) == S.SAGE_ERR_ARG
     assert call(groups=9) == S.SAGE_ERR_ARG                     # more ranges than heads
