@@ -235,10 +235,12 @@ typedef struct {
  * `stream`, without synchronizing.
  *  q_len, kv_len : HOST int32 [B] valid lengths (clamped to [0, Nq] and
  *                  [0, Nkv]), or NULL for all rows valid.  They are copied
- *                  into the lengths slot at the end of buf->workspace before
- *                  the call returns, so the arrays may be reused at once.
- *                  Rows >= q_len[b] of the device output are not written;
- *                  the `output` region is copied back as given. */
+ *                  on `stream` into the lengths slot at the end of
+ *                  buf->workspace.  Pageable arrays are staged before the
+ *                  call returns and may be reused at once; pinned arrays are
+ *                  read when the stream reaches the copy and must not change
+ *                  before then.  Rows >= q_len[b] of the device output are
+ *                  not written; the `output` region is copied back as given. */
 int sage_attention_host(const sage_copy* inputs, int n_inputs,
                         const sage_tensor* q, const sage_tensor* k, const sage_tensor* v,
                         const sage_prep_buffers* buf, const sage_tensor* o,

@@ -5,7 +5,6 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
-#include <vector>
 
 #include "sage_gb300.h"
 #include "sage_internal.h"
@@ -407,17 +406,20 @@ int sage_attention(const sage_tensor* q, const sage_tensor* k, const sage_tensor
     return rc;
 }
 
-// Host-memory entries: stage per-item lengths given as host arrays (NULL:
-// all valid; values clamped to [0, n]) into the workspace's lengths slot on
-// `s`.  Fills the clamped values into lq/lk (host) and points *q_dev/*kv_dev
-// at the device copies (NULL when the host array was NULL).
+// A host length clamped to [0, n] (NULL array: n), as the kernels clamp
+// the device copies.
+static int host_len(const int32_t* lens, int b, int n) {
+    if (lens == nullptr) return n;
+    return lens[b] < 0 ? 0 : (lens[b] > n ? n : lens[b]);
+}
+
+// Host-memory entries: stage per-item lengths given as host arrays (NULL: all
+// valid) into the workspace's lengths slot on `s`, and point *q_dev/*kv_dev
+// at the device copies (NULL when the host array was NULL).  The kernels
+// clamp the staged values.
 static int stage_host_lens(const sage_prep_buffers* buf, int B, int H, int Nq, int Nkv, int D,
-                           const int32_t* q_len, const int32_t* kv_len, cudaStream_t s, int32_t* lq,
-                           int32_t* lk, const int32_t** q_dev, const int32_t** kv_dev) {
-    for (int b = 0; b < B; ++b) {
-        lq[b] = q_len ? (q_len[b] < 0 ? 0 : (q_len[b] > Nq ? Nq : q_len[b])) : Nq;
-        lk[b] = kv_len ? (kv_len[b] < 0 ? 0 : (kv_len[b] > Nkv ? Nkv : kv_len[b])) : Nkv;
-    }
+                           const int32_t* q_len, const int32_t* kv_len, cudaStream_t s,
+                           const int32_t** q_dev, const int32_t** kv_dev) {
     *q_dev = *kv_dev = nullptr;
     if (q_len == nullptr && kv_len == nullptr) return SAGE_OK;
     if (buf == nullptr || buf->workspace == nullptr) return SAGE_ERR_ARG;
@@ -426,8 +428,8 @@ static int stage_host_lens(const sage_prep_buffers* buf, int B, int H, int Nq, i
     if (buf->workspace_bytes < sz.workspace) return SAGE_ERR_ARG;
     int32_t* slot = prep_lens_slot(buf->workspace, B, H, ceil_div(Nkv, kMeanChunk), D);
     // pageable sources: the copies are staged before cudaMemcpyAsync returns
-    if (cudaMemcpyAsync(slot, lq, sizeof(int32_t) * B, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaMemcpyAsync(slot + B, lk, sizeof(int32_t) * B, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    if ((q_len && cudaMemcpyAsync(slot, q_len, sizeof(int32_t) * B, cudaMemcpyHostToDevice, s) != cudaSuccess) ||
+        (kv_len && cudaMemcpyAsync(slot + B, kv_len, sizeof(int32_t) * B, cudaMemcpyHostToDevice, s) != cudaSuccess))
         return SAGE_ERR_LAUNCH;
     if (q_len) *q_dev = slot;
     if (kv_len) *kv_dev = slot + B;
@@ -442,11 +444,8 @@ int sage_attention_host(const sage_copy* inputs, int n_inputs, const sage_tensor
     int rc = check_shape(B, H, Nq, Nkv, D);
     if (rc != SAGE_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    std::vector<int32_t> lq(B), lk(B);
     const int32_t *q_dev = nullptr, *kv_dev = nullptr;
-    if ((rc = stage_host_lens(buf, B, H, Nq, Nkv, D, q_len, kv_len, s, lq.data(), lk.data(), &q_dev, &kv_dev)) !=
-        SAGE_OK)
-        return rc;
+    if ((rc = stage_host_lens(buf, B, H, Nq, Nkv, D, q_len, kv_len, s, &q_dev, &kv_dev)) != SAGE_OK) return rc;
     for (int i = 0; i < n_inputs; ++i) {
         if (!inputs[i].host || !inputs[i].device) return SAGE_ERR_ARG;
         if (cudaMemcpyAsync(inputs[i].device, inputs[i].host, inputs[i].bytes, cudaMemcpyHostToDevice, s) !=
@@ -466,14 +465,14 @@ int sage_attention_host(const sage_copy* inputs, int n_inputs, const sage_tensor
     return SAGE_OK;
 }
 
-// Copy rows [0, rows[b]) of heads [h0, h0 + nh) of a [B, H, N, D] BF16 tensor
-// (element strides of t; the same physical layout on both sides) with 2-D
-// copies.
-static int copy_heads(void* dst, const void* src, const sage_tensor* t, int B, const int32_t* rows, int D, int h0,
-                      int nh, cudaMemcpyKind kind, cudaStream_t s) {
+// Copy rows [0, host_len(lens, b, n)) of heads [h0, h0 + nh) of a [B, H, n, D]
+// BF16 tensor (element strides of t; the same physical layout on both sides)
+// with 2-D copies.
+static int copy_heads(void* dst, const void* src, const sage_tensor* t, int B, const int32_t* lens, int n, int D,
+                      int h0, int nh, cudaMemcpyKind kind, cudaStream_t s) {
     const int64_t sb = t->stride_b, sh = t->stride_h, sn = t->stride_n;
     for (int b = 0; b < B; ++b) {
-        const int N = rows[b];
+        const int N = host_len(lens, b, n);
         if (N <= 0) continue;
         const int64_t off = (b * sb + (int64_t)h0 * sh) * 2;
         char* d = static_cast<char*>(dst) + off;
@@ -538,11 +537,8 @@ int sage_attention_host_overlapped(const sage_tensor* q_host, const sage_tensor*
     OverlapStreams* os = overlap_streams();
     if (os == nullptr) return SAGE_ERR_LAUNCH;
     cudaStream_t user = static_cast<cudaStream_t>(stream);
-    std::vector<int32_t> lq(B), lk(B);
     const int32_t *q_dev = nullptr, *kv_dev = nullptr;
-    if ((rc = stage_host_lens(buf, B, H, Nq, Nkv, D, q_len, kv_len, user, lq.data(), lk.data(), &q_dev, &kv_dev)) !=
-        SAGE_OK)
-        return rc;
+    if ((rc = stage_host_lens(buf, B, H, Nq, Nkv, D, q_len, kv_len, user, &q_dev, &kv_dev)) != SAGE_OK) return rc;
     if (cudaEventRecord(os->start, user) != cudaSuccess) return SAGE_ERR_LAUNCH;
     for (int i = 0; i < 3; ++i)
         if (cudaStreamWaitEvent(os->s[i], os->start, 0) != cudaSuccess) return SAGE_ERR_LAUNCH;
@@ -550,11 +546,11 @@ int sage_attention_host_overlapped(const sage_tensor* q_host, const sage_tensor*
     for (int g = 0; g < head_groups && rc == SAGE_OK; ++g) {
         const int h0 = (int)((int64_t)H * g / head_groups), h1 = (int)((int64_t)H * (g + 1) / head_groups);
         cudaStream_t s = os->s[g % 3];
-        if ((rc = copy_heads(const_cast<void*>(q->ptr), q_host->ptr, q, B, lq.data(), D, h0, h1 - h0,
+        if ((rc = copy_heads(const_cast<void*>(q->ptr), q_host->ptr, q, B, q_len, Nq, D, h0, h1 - h0,
                              cudaMemcpyHostToDevice, s)) != SAGE_OK ||
-            (rc = copy_heads(const_cast<void*>(k->ptr), k_host->ptr, k, B, lk.data(), D, h0, h1 - h0,
+            (rc = copy_heads(const_cast<void*>(k->ptr), k_host->ptr, k, B, kv_len, Nkv, D, h0, h1 - h0,
                              cudaMemcpyHostToDevice, s)) != SAGE_OK ||
-            (rc = copy_heads(const_cast<void*>(v->ptr), v_host->ptr, v, B, lk.data(), D, h0, h1 - h0,
+            (rc = copy_heads(const_cast<void*>(v->ptr), v_host->ptr, v, B, kv_len, Nkv, D, h0, h1 - h0,
                              cudaMemcpyHostToDevice, s)) != SAGE_OK)
             break;
         rc = prep_common(q, k, v, B, H, Nq, Nkv, D, q_dev, kv_dev, kSV, buf, s, h0, h1 - h0);
@@ -564,7 +560,7 @@ int sage_attention_host_overlapped(const sage_tensor* q_host, const sage_tensor*
                          nullptr, false, h0, h1 - h0);
         if (rc != SAGE_OK) break;
         launches += g_last_launches;
-        rc = copy_heads(const_cast<void*>(o_host->ptr), o->ptr, o, B, lq.data(), D, h0, h1 - h0,
+        rc = copy_heads(const_cast<void*>(o_host->ptr), o->ptr, o, B, q_len, Nq, D, h0, h1 - h0,
                         cudaMemcpyDeviceToHost, s);
     }
     // the caller's stream resumes after every group, also on an error
