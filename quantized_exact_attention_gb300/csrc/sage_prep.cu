@@ -545,6 +545,9 @@ __global__ void __launch_bounds__(256, kPrepCtasPerSm) prep_onepass_kernel(const
 std::atomic<uint32_t> g_prep_epoch{0};
 
 template <int D>
+cudaError_t launch_prep_d(const PrepParams& p, bool with_q, cudaStream_t s, int* launches);
+
+template <int D>
 cudaError_t launch_prep_onepass(const PrepParams& p, bool with_q, cudaStream_t s, int* launches) {
     using Sh = PrepShape<D>;
     static int grid_max[64] = {};
@@ -558,8 +561,10 @@ cudaError_t launch_prep_onepass(const PrepParams& p, bool with_q, cudaStream_t s
             return e;
         grid_max[dev] = n * (per > 0 ? per : 1);
     }
+    const int64_t heads = (int64_t)p.B * p.h_count;
+    if (heads > (1 << 24)) return launch_prep_d<D>(p, with_q, s, launches);   // queue indices stay in int
     PrepQueue q{};
-    q.nheads = p.B * p.h_count;
+    q.nheads = (int)heads;
     q.nS = (p.n_chunks + Sh::kStatChunks - 1) / Sh::kStatChunks;
     q.nQ = with_q ? (p.nq_blocks + kItemBlocks - 1) / kItemBlocks : 0;
     q.nK = (p.nk_blocks + kItemBlocks - 1) / kItemBlocks;
