@@ -492,6 +492,15 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 }
             }
             tmem_wait_st();
+            // P-ready first: the PV MMA needs only P; the alpha hand-off to the
+            // correction (which may wait for its slot) follows
+            tc_fence_before();
+            if constexpr (kPair) {                          // one arrival per warp, on rank 0's barrier
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(mapa_rank(bar(B_PFULL + s3), 0));
+            } else {
+                mbar_arrive(bar(B_PFULL + s3));
+            }
             if (half == 0) {
                 if (t >= 2 && !wwait(bar(B_AFREE + sb), ((t >> 1) - 1) & 1, abort_flag)) {
                     if (lane == 0) fail(R_SOFTMAX, t);
@@ -500,15 +509,8 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 }
                 alpha_s[(sb * 2) * 128 + row] = alpha;
                 if (kB64) alpha_s[(sb * 2 + 1) * 128 + row] = alpha_b;
+                mbar_arrive(bar(B_AFULL + sb));
             }
-            tc_fence_before();
-            if constexpr (kPair) {                          // one arrival per warp, on rank 0's barrier
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(mapa_rank(bar(B_PFULL + s3), 0));
-            } else {
-                mbar_arrive(bar(B_PFULL + s3));
-            }
-            if (half == 0) mbar_arrive(bar(B_AFULL + sb));
             if constexpr (kB64) {
                 // half 0's keys join in epoch A, half 1's in epoch B
                 l_run = half == 0 ? __fmul_rn(fmaf(l_run, alpha, tile_sum), alpha_b)
