@@ -69,8 +69,8 @@ enum Bar : uint32_t {
     B_PFULL = B_SFREE + kNS,
     B_PVFULL = B_PFULL + kNS,   // PV buffer 0 (the only one except with BKV = 64)
     B_PVFREE = B_PVFULL + 1,
-    B_AFULL = B_PVFREE + 1,
-    B_AFREE = B_AFULL + 2,
+    B_AFULL = B_PVFREE + 1,     // [4]: alpha slots (the BKV = 64 and paired forms use two)
+    B_AFREE = B_AFULL + 4,      // [2]: alpha slot read (BKV = 64 and paired forms)
     B_XM = B_AFREE + 2,         // [buf][quarter]: the two halves of 32 rows exchanged maxima
     B_LFULL = B_XM + 8,
     B_DRAIN = B_LFULL + 1,
@@ -95,7 +95,7 @@ struct Smem {
     static constexpr uint32_t OFF_K = OFF_Q + kTileQBytes;
     static constexpr uint32_t OFF_V = OFF_K + kNK * kTileKBytes;
     static constexpr uint32_t OFF_BAR = OFF_V + kNV * kTileVBytes;
-    static constexpr uint32_t OFF_ALPHA = OFF_BAR + ((B_COUNT * 8 + 15) / 16) * 16;   // float [2 buf][2 epoch][128]
+    static constexpr uint32_t OFF_ALPHA = OFF_BAR + ((B_COUNT * 8 + 15) / 16) * 16;   // float [4 slot][128] or [2 buf][2 epoch][128]
     static constexpr uint32_t OFF_XM = OFF_ALPHA + 4 * 128 * 4;                       // float [2 buf][2 half][128]
     static constexpr uint32_t OFF_L = OFF_XM + 4 * 128 * 4;                           // float [2 half][128]
     static constexpr uint32_t OFF_VS = OFF_L + 2 * 128 * 4;                           // float [D]
@@ -246,6 +246,18 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // epoch e waits only for the drain of epoch e of the previous tile; the
     // S/P buffers are then two.
     constexpr bool kDB = kB64 && !kPair;
+    // The MMA issuer's order makes two handshakes implied in the one-CTA
+    // forms that issue PV:
+    // - S-free: QK(t+2) reuses the S/P buffer of tile t-1, and the same
+    //   thread issued PV(t-1) after P-full(t-1), which the softmax arrives
+    //   only once it has read S(t-1).  (The capture form issues no PV and
+    //   keeps the handshake; the BKV = 64 form never needed it.)
+    // - alpha-free, with four alpha slots: the correction reads alpha(t)
+    //   before it arrives PV-free(t); PV(t+1) waits for that, QK(t+4) is
+    //   issued after PV(t+1), and the softmax writes alpha(t+4) only after
+    //   S-full(t+4).
+    constexpr bool kSFree = kCapture;
+    constexpr bool kRing4 = !kB64 && !kPair;
     static_assert(!(kB64 && kFusedQ), "the BKV = 64 form has no fused Q prologue (its scratch holds PV barriers)");
     constexpr int kNSb = kDB ? 2 : kNS;
     auto tm_pv = [&](int j) -> uint32_t { return kDB ? 256u + 128u * (uint32_t)j : TM_PV; };
@@ -275,10 +287,8 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             mbar_init(pv_free(1), 256);
         }
         for (int i = 0; i < 8; ++i) mbar_init(bar(B_XM + i), 64);    // both halves of 32 rows
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(B_AFULL + i), 128);     // softmax half 0 (writes alpha)
-            mbar_init(bar(B_AFREE + i), 256);     // every correction thread
-        }
+        for (int i = 0; i < 4; ++i) mbar_init(bar(B_AFULL + i), 128);   // softmax half 0 (writes alpha)
+        for (int i = 0; i < 2; ++i) mbar_init(bar(B_AFREE + i), 256);   // every correction thread
         mbar_init(bar(B_LFULL), 256);             // every softmax thread
         mbar_init(bar(B_DRAIN), 1);
         mbar_init(bar(B_QREADY), 512);            // every softmax and correction thread (fused Q)
@@ -384,7 +394,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             tmem_ld32(tmem + lane_base + TM_S + s3 * 128 + half * 64 + 32, s1);
             tmem_wait_ld();
             tc_fence_before();
-            mbar_arrive(bar(B_SFREE + s3));
+            if constexpr (kSFree) mbar_arrive(bar(B_SFREE + s3));
             // valid columns of this half (may be <= 0); causal: per row
             const int lim = (kCausal ? min(lk, q0 + row + diag + 1) : lk) - t * 128 - half * 64;
             const bool full = kCausal ? __all_sync(0xffffffffu, lim >= 64) : (lim >= 64);
@@ -502,14 +512,19 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 mbar_arrive(bar(B_PFULL + s3));
             }
             if (half == 0) {
-                if (t >= 2 && !wwait(bar(B_AFREE + sb), ((t >> 1) - 1) & 1, abort_flag)) {
-                    if (lane == 0) fail(R_SOFTMAX, t);
-                    ok = false;
-                    break;
+                if constexpr (kRing4) {
+                    alpha_s[(t & 3) * 128 + row] = alpha;
+                    mbar_arrive(bar(B_AFULL + (t & 3)));
+                } else {
+                    if (t >= 2 && !wwait(bar(B_AFREE + sb), ((t >> 1) - 1) & 1, abort_flag)) {
+                        if (lane == 0) fail(R_SOFTMAX, t);
+                        ok = false;
+                        break;
+                    }
+                    alpha_s[(sb * 2) * 128 + row] = alpha;
+                    if (kB64) alpha_s[(sb * 2 + 1) * 128 + row] = alpha_b;
+                    mbar_arrive(bar(B_AFULL + sb));
                 }
-                alpha_s[(sb * 2) * 128 + row] = alpha;
-                if (kB64) alpha_s[(sb * 2 + 1) * 128 + row] = alpha_b;
-                mbar_arrive(bar(B_AFULL + sb));
             }
             if constexpr (kB64) {
                 // half 0's keys join in epoch A, half 1's in epoch B
@@ -539,14 +554,16 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             bool ok = true;
             for (int t = 0; t < T; ++t) {
                 const int sb = t & 1;
-                if (!__all_sync(0xffffffffu, swait(bar(B_AFULL + sb), (t >> 1) & 1, abort_flag))) {
+                const bool got_alpha = kRing4 ? swait(bar(B_AFULL + (t & 3)), (t >> 2) & 1, abort_flag)
+                                              : swait(bar(B_AFULL + sb), (t >> 1) & 1, abort_flag);
+                if (!__all_sync(0xffffffffu, got_alpha)) {
                     if (lane == 0) fail(R_CORRECT, t);
                     ok = false;
                     break;
                 }
-                const float alpha_a = alpha_s[(sb * 2) * 128 + row];
+                const float alpha_a = kRing4 ? alpha_s[(t & 3) * 128 + row] : alpha_s[(sb * 2) * 128 + row];
                 const float alpha_b = kB64 ? alpha_s[(sb * 2 + 1) * 128 + row] : 1.f;
-                mbar_arrive(bar(B_AFREE + sb));
+                if constexpr (!kRing4) mbar_arrive(bar(B_AFREE + sb));
 #pragma unroll 1
                 for (int e = 0; e < (kB64 ? 2 : 1); ++e) {  // PV epochs of this tile
                     const float alpha = e ? alpha_b : alpha_a;
@@ -755,9 +772,8 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // whose P the PV MMA issued before it (same thread, in order) reads.
             auto issue_qk = [&](int t) -> bool {
                 if (!bwait(bar(B_KFULL + k_st), k_ph, abort_flag)) return false;
-                // kDB: P-ready of the tile that used this buffer, waited before its
-                // PV, already implies that the softmax has read its S
-                if (!kDB && t >= kNS && !bwait(bar(B_SFREE + qb), qph ^ 1, abort_flag)) return false;
+                // only the capture form waits for S-free (see kSFree)
+                if (kSFree && t >= kNS && !bwait(bar(B_SFREE + qb), qph ^ 1, abort_flag)) return false;
                 tc_fence_after();
                 const uint64_t bK = dK + (uint64_t)(k_st * (kTileKBytes >> 4));
                 const uint32_t dS = tmem + TM_S + qb * 128;
