@@ -246,18 +246,28 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // epoch e waits only for the drain of epoch e of the previous tile; the
     // S/P buffers are then two.
     constexpr bool kDB = kB64 && !kPair;
-    // The MMA issuer's order makes two handshakes implied in the one-CTA
-    // forms that issue PV:
-    // - S-free: QK(t+2) reuses the S/P buffer of tile t-1, and the same
-    //   thread issued PV(t-1) after P-full(t-1), which the softmax arrives
-    //   only once it has read S(t-1).  (The capture form issues no PV and
-    //   keeps the handshake; the BKV = 64 form never needed it.)
-    // - alpha-free, with four alpha slots: the correction reads alpha(t)
-    //   before it arrives PV-free(t); PV(t+1) waits for that, QK(t+4) is
-    //   issued after PV(t+1), and the softmax writes alpha(t+4) only after
-    //   S-full(t+4).
+    // The MMA issuer's order makes four handshakes implied in the one-CTA
+    // forms:
+    // - S-free (forms that issue PV): QK(t+2) reuses the S/P buffer of tile
+    //   t-1, and the same thread issued PV(t-1) after P-full(t-1), which the
+    //   softmax arrives only once it has read S(t-1).  The capture form issues
+    //   no PV and keeps the handshake; the BKV = 64 form never needed it.
+    // - alpha-free (forms with one alpha per tile), with four alpha slots: the
+    //   correction reads alpha(t) before it arrives PV-free(t); PV(t+1) waits
+    //   for that, QK(t+4) is issued after PV(t+1), and the softmax writes
+    //   alpha(t+4) only after S-full(t+4).
+    // - K-empty (three S/P buffers): a K stage is free once the QK that read it
+    //   has completed, and with as many S/P buffers as K stages that QK's
+    //   commit is S-full of the same index; the producer waits on it.
+    // - V-empty (one PV commit per tile): a V stage is free once PV of the
+    //   tile that used it has completed, i.e. at PV-full of that tile.  The
+    //   single PV-full barrier may have run ahead of the producer by one more
+    //   phase, in which case the producer waits one tile longer than needed;
+    //   PV(t-1) never depends on V(t), so it cannot wait forever.
     constexpr bool kSFree = kCapture;
     constexpr bool kRing4 = !kB64 && !kPair;
+    constexpr bool kKSlotBySFull = !kDB && !kPair && (kNS == kNK);
+    constexpr bool kVSlotByPVFull = !kB64 && !kPair && !kCapture;
     static_assert(!(kB64 && kFusedQ), "the BKV = 64 form has no fused Q prologue (its scratch holds PV barriers)");
     constexpr int kNSb = kDB ? 2 : kNS;
     auto tm_pv = [&](int j) -> uint32_t { return kDB ? 256u + 128u * (uint32_t)j : TM_PV; };
@@ -696,7 +706,9 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
             auto load_k = [&](int t) -> bool {
                 const int st = t % kNK;
-                if (t >= kNK && !swait(bar(B_KEMPTY + st), ((t / kNK) - 1) & 1, abort_flag)) return false;
+                if (t >= kNK && !swait(kKSlotBySFull ? bar(B_SFULL + st) : bar(B_KEMPTY + st), ((t / kNK) - 1) & 1,
+                                       abort_flag))
+                    return false;
                 const uint32_t dst = sbase + OFF_K + st * kTileKBytes;
                 if (rank == 0) mbar_arrive_expect_tx(bar(B_KFULL + st), (kPair ? 2 : 1) * kTileKBytes);
 #pragma unroll
@@ -712,7 +724,9 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             };
             auto load_v = [&](int t) -> bool {
                 const int st = t % kNV;
-                if (t >= kNV && !swait(bar(B_VEMPTY + st), ((t / kNV) - 1) & 1, abort_flag)) return false;
+                if (t >= kNV && !swait(kVSlotByPVFull ? bar(B_PVFULL) : bar(B_VEMPTY + st),
+                                       kVSlotByPVFull ? ((t - kNV) & 1) : (((t / kNV) - 1) & 1), abort_flag))
+                    return false;
                 const uint32_t dst = sbase + OFF_V + st * kTileVBytes;
                 if (rank == 0) mbar_arrive_expect_tx(bar(B_VFULL + st), (kPair ? 2 : 1) * kTileVBytes);
                 if (p.fault_mode != 1) {
@@ -787,7 +801,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         mma_f16_ss(dS, dQ + off_a, bK + off_b, kIdescQK, kk > 0 ? 1u : 0u);
                 }
                 commit(bar(B_SFULL + qb));
-                commit(bar(B_KEMPTY + k_st));
+                if constexpr (!kKSlotBySFull) commit(bar(B_KEMPTY + k_st));
                 if (++k_st == kNK) { k_st = 0; k_ph ^= 1; }
                 if (++qb == kNSb) { qb = 0; qph ^= 1; }
                 return true;
@@ -820,7 +834,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     }
                     commit(pv_full(pj));
                 }
-                commit(bar(B_VEMPTY + v_st));
+                if constexpr (!kVSlotByPVFull) commit(bar(B_VEMPTY + v_st));
                 if (++v_st == kNV) { v_st = 0; v_ph ^= 1; }
                 if (++pb == kNSb) { pb = 0; pph ^= 1; }
                 return true;
