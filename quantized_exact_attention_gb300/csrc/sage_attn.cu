@@ -399,9 +399,17 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 break;
             }
             tc_fence_after();
+            // The half row's 64 scores; every form but the capture takes their
+            // maximum from the load itself (tcgen05.ld.red), which replaces a
+            // 16-instruction max loop on the softmax's critical chain.
             uint32_t s0[32], s1[32];
-            tmem_ld32(tmem + lane_base + TM_S + s3 * 128 + half * 64, s0);
-            tmem_ld32(tmem + lane_base + TM_S + s3 * 128 + half * 64 + 32, s1);
+            float mx_ld = -INFINITY;
+            if constexpr (kCapture) {
+                tmem_ld32(tmem + lane_base + TM_S + s3 * 128 + half * 64, s0);
+                tmem_ld32(tmem + lane_base + TM_S + s3 * 128 + half * 64 + 32, s1);
+            } else {
+                tmem_ld64_max(tmem + lane_base + TM_S + s3 * 128 + half * 64, s0, s1, mx_ld);
+            }
             tmem_wait_ld();
             tc_fence_before();
             if constexpr (kSFree) mbar_arrive(bar(B_SFREE + s3));
@@ -422,18 +430,11 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 continue;
             }
 
-            // half-row maximum of the raw integer scores
+            // half-row maximum of the raw integer scores: the load's own when
+            // all 64 columns are valid, else over the valid columns only
             float mx;
             if (full) {
-                float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
-#pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    a0 = fmax3(a0, __uint_as_float(s0[i]), __uint_as_float(s0[i + 1]));
-                    a1 = fmax3(a1, __uint_as_float(s0[i + 2]), __uint_as_float(s0[i + 3]));
-                    a2 = fmax3(a2, __uint_as_float(s1[i]), __uint_as_float(s1[i + 1]));
-                    a3 = fmax3(a3, __uint_as_float(s1[i + 2]), __uint_as_float(s1[i + 3]));
-                }
-                mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+                mx = mx_ld;
             } else {
                 mx = -INFINITY;
 #pragma unroll
