@@ -229,11 +229,14 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if constexpr (kPair) return mbar_wait_cluster(bb, par, af);
         else return mbar_wait(bb, par, af);
     };
+    // A wait taken by all 32 lanes of a warp: one warp-wide vote per poll.
     auto wwait = [&](uint32_t bb, uint32_t par, const volatile int* af) -> bool {
-        return __all_sync(0xffffffffu, bwait(bb, par, af));
+        if constexpr (kPair) return __all_sync(0xffffffffu, bwait(bb, par, af));
+        else return mbar_wait_warp(bb, par, af);
     };
-    // Waits off the critical chain (the correction's alpha wait, the producer's
-    // ring-slot waits) sleep between checks; the others spin.
+    // Waits off the critical chain (the producer's ring-slot waits, the alpha
+    // wait of the BKV = 64 and paired forms) sleep between checks; the others
+    // spin.
     auto swait = [&](uint32_t bb, uint32_t par, const volatile int* af) -> bool {
         if constexpr (kPair) return mbar_wait_cluster(bb, par, af);
         else return mbar_wait_sleep(bb, par, af);
@@ -565,7 +568,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             bool ok = true;
             for (int t = 0; t < T; ++t) {
                 const int sb = t & 1;
-                const bool got_alpha = kRing4 ? swait(bar(B_AFULL + (t & 3)), (t >> 2) & 1, abort_flag)
+                const bool got_alpha = kRing4 ? wwait(bar(B_AFULL + (t & 3)), (t >> 2) & 1, abort_flag)
                                               : swait(bar(B_AFULL + sb), (t >> 1) & 1, abort_flag);
                 if (!__all_sync(0xffffffffu, got_alpha)) {
                     if (lane == 0) fail(R_CORRECT, t);
@@ -580,6 +583,13 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     const float alpha = e ? alpha_b : alpha_a;
                     const bool unit = __all_sync(0xffffffffu, alpha == 1.0f);   // RN(RO * 1) == RO
                     const int pj = kDB ? e : 0;                 // PV buffer of this epoch
+                    // RO = RN(RN(RO * alpha) + PV16): the product first, as one
+                    // warp-uniform block skipped when alpha is 1 for the whole
+                    // warp, and before the wait for PV
+                    if (!unit) {
+#pragma unroll
+                        for (int i = 0; i < kDH; i += 2) mul2_s(ro[i], ro[i + 1], alpha);
+                    }
                     if (!wwait(pv_full(pj), kDB ? (t & 1) : (kB64 ? e : (t & 1)), abort_flag)) {
                         if (lane == 0) fail(R_CORRECT, t);
                         ok = false;
@@ -607,13 +617,7 @@ sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                             for (int i = 0; i < 4; ++i) dp[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
                         }
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            // RO = RN(RN(RO * alpha) + PV16)
-                            float& r0 = ro[c * 32 + 2 * i];
-                            float& r1 = ro[c * 32 + 2 * i + 1];
-                            if (!unit) mul2_s(r0, r1, alpha);
-                            add_f16x2_to(r0, r1, v[i]);
-                        }
+                        for (int i = 0; i < 16; ++i) add_f16x2_to(ro[c * 32 + 2 * i], ro[c * 32 + 2 * i + 1], v[i]);
                     }
                 }
                 if (!ok) break;

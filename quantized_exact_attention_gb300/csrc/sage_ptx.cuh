@@ -63,6 +63,21 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
     }
 }
 
+// The same bounded wait taken by a whole warp: each poll is one warp-wide
+// vote, so the loop is uniform over the warp and every lane returns the same
+// result.  All 32 lanes must call it together.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+        if ((i & 63u) == 0) {
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) return false;
+            if (__any_sync(0xffffffffu, globaltimer() - t0 > kWaitLimitNs)) return false;
+        }
+    }
+}
+
 // The same bounded wait with a suspend-time hint: between checks the thread
 // may sleep until the phase completes (or 200 ns pass), so its polling does
 // not take issue slots from the warps it shares a scheduler with.  Waking
